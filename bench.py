@@ -1,0 +1,412 @@
+#!/usr/bin/env python3
+"""Throughput of exact attention (forward + backward) on GB300.
+
+One step is one pass of the whole hot path over one batch of the causal
+N=4096, d=128 workload (B=2, H=32, 1% of Q and K rows scaled x20): the
+forward kernel, then the three backward stages (prepare, main, finish) --
+exactly the launches fattn_fwd + fattn_bwd make.  FLOPs are counted as
+4*B*H*N^2*d for the forward, x2.5 for the backward, halved for causal.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fattn|reference]
+
+With torchrun (N > 1) every rank runs an independent replica of the
+workload on its own GPU (attention over (batch, head) needs no exchange),
+the timed region is bracketed by barriers and the max time over ranks is
+used.  Rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle on the host cores instead (one
+head of the workload per step), on the same metric.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOP/s and fraction of GB300 dense BF16 peak"
+DEFAULT_WORKLOAD = "b2h32_n4096_d128_causal_outliers"
+KERNEL_SOURCES = {
+    "fwd": "exact_attention_fattn_gb300/csrc/fattn_fwd.cu",
+    "bwd_main": "exact_attention_fattn_gb300/csrc/fattn_bwd.cu",
+    "bwd_prepare": "exact_attention_fattn_gb300/csrc/fattn_bwd_aux.cu",
+    "bwd_finish": "exact_attention_fattn_gb300/csrc/fattn_bwd_aux.cu",
+}
+L2_BYTES = 129 * 10**6
+
+
+def flop_counts(w):
+    base = 4.0 * w.B * w.H * w.N * w.N * w.d * (0.5 if w.causal else 1.0)
+    return base, 2.5 * base
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16": float(p["bf16_tflops"]), "bf16_sustained": float(p["bf16_tflops_sustained"]),
+                "hbm": float(p["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+def source_hash(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed after the capture."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload:
+                    if parts[3] == source_hash(KERNEL_SOURCES[kernel]):
+                        return float(parts[2])
+                    return None
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples, time-stamped on the host."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                self.samples.append((time.time(), float(parts[1]), float(parts[2]), parts[4:9]))
+            except ValueError:
+                continue
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed_region"
+        if not inside and self.samples:
+            mid = 0.5 * (t0 + t1)
+            inside = sorted(self.samples, key=lambda s: abs(s[0] - mid))[:3]
+            window = "nearest_to_timed_region"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for s in inside:
+            for name, flag in zip(names, s[3][1:]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s[1] for s in inside),
+                "sm_max_mhz": max(s[2] for s in inside), "reasons": sorted(reasons),
+                "samples": len(inside), "window": window}
+
+
+def cpu_baseline(w, heads: int):
+    """The fp64 oracle, as it stands, on `heads` (b, h) slices of the
+    workload: full forward + backward of each slice on the host cores."""
+    import oracle
+    from exact_attention_fattn_gb300 import workloads as W
+
+    inp = W.make_inputs(w)
+    base, bwd = flop_counts(w)
+    per_head = (base + bwd) / (w.B * w.H)
+    t0 = time.perf_counter()
+    for hflat in range(heads):
+        b, h = divmod(hflat, w.H)
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        sub = {n: inp[n][sl] for n in ("q", "k", "v", "do")}
+        oracle.attention_forward(sub["q"], sub["k"], sub["v"], w.causal, w.scale)
+        oracle.attention_backward(sub["q"], sub["k"], sub["v"], sub["do"], w.causal, w.scale)
+    dt = time.perf_counter() - t0
+    return {"value": per_head * heads / dt / 1e12, "unit": "TFLOP/s",
+            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{heads} of {w.B * w.H} heads of {w.name}: fp64 forward + backward "
+                      f"({dt:.1f} s; BLAS threads at their default)",
+            "seconds": dt}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from exact_attention_fattn_gb300 import workloads as W
+
+    inp = W.make_inputs(w)
+    base, bwd = flop_counts(w)
+    per_head = (base + bwd) / (w.B * w.H)
+    nheads = w.B * w.H
+
+    def step(k):
+        b, h = divmod(k % nheads, w.H)
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        sub = {n: inp[n][sl] for n in ("q", "k", "v", "do")}
+        oracle.attention_forward(sub["q"], sub["k"], sub["v"], w.causal, w.scale)
+        oracle.attention_backward(sub["q"], sub["k"], sub["v"], sub["do"], w.causal, w.scale)
+
+    for k in range(args.warmup):
+        step(k)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        step(args.warmup + k)
+    dt = time.perf_counter() - t0
+    value = per_head * args.steps / dt / 1e12
+    cores = len(os.sched_getaffinity(0))
+    sample = f"one (b, h) head of {w.name} per step, rotating over heads; fp64 forward + backward"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_fattn(args, w):
+    import torch
+
+    from exact_attention_fattn_gb300 import attention as A
+    from exact_attention_fattn_gb300 import workloads as W
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    # replicas only: each rank draws its own batch of the same workload
+    inp = W.make_inputs(w, seed=w.seed + 7919 * rank)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = A.workspace_for(q)
+    sc = w.scale
+
+    def fwd():
+        A.fattn_fwd(q, k, v, causal=w.causal, scale=sc, out=o, lse=lse)
+
+    def prep():
+        A.fattn_bwd_prepare(o, do, lse, ws)
+
+    def main():
+        A.fattn_bwd_main(q, k, v, do, ws, dk, dv, causal=w.causal, scale=sc)
+
+    def finish():
+        A.fattn_bwd_finish(ws, dq, scale=sc)
+
+    stages = [("fwd", fwd), ("bwd_prepare", prep), ("bwd_main", main), ("bwd_finish", finish)]
+    for _ in range(args.warmup):
+        for _, fn in stages:
+            fn()
+    status = A.fattn_check_status(dev)
+    if status != 0:
+        raise RuntimeError(f"libfattn reported status {status} during warm-up")
+
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = str(local)
+    sampler = ClockSampler(uuid)
+    time.sleep(0.3)
+
+    stream = torch.cuda.current_stream(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+          for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_host0 = time.time()
+    start.record(stream)
+    for s in range(args.steps):
+        ev[s][0].record(stream)
+        for i, (_, fn) in enumerate(stages):
+            fn()
+            ev[s][i + 1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_host1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    status = A.fattn_check_status(dev)
+    if status != 0:
+        raise RuntimeError(f"libfattn reported status {status} in the timed region")
+    per_stage = {name: statistics.mean(ev[s][i].elapsed_time(ev[s][i + 1])
+                                       for s in range(args.steps))
+                 for i, (name, _) in enumerate(stages)}
+    time.sleep(0.2)
+    sampler.stop()
+    clocks = sampler.summary(t_host0, t_host1)
+
+    # ---- end to end through the public API: pinned host buffers in, results out
+    e2e = None
+    if not args.no_e2e:
+        host_in = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
+        host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                    for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+        def e2e_step():
+            for n, t in zip(("q", "k", "v", "do"), (q, k, v, do)):
+                t.copy_(host_in[n], non_blocking=True)
+            A.fattn_fwd(q, k, v, causal=w.causal, scale=sc, out=o, lse=lse)
+            A.fattn_bwd(q, k, v, o, do, lse, causal=w.causal, scale=sc, workspace=ws,
+                        dq=dq, dk=dk, dv=dv)
+            for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+                host_out[n].copy_(t, non_blocking=True)
+
+        e2e_steps = max(3, min(args.steps, 50))
+        for _ in range(3):
+            e2e_step()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        base, bwd = flop_counts(w)
+        e2e = {"value": world * (base + bwd) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "steps": e2e_steps}
+        if A.fattn_check_status(dev) != 0:
+            raise RuntimeError("libfattn reported an error in the end-to-end run")
+
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+
+    peaks = load_peaks()
+    base, bwd = flop_counts(w)
+    ms_step = total_ms / args.steps
+    value = world * (base + bwd) / (ms_step * 1e-3) / 1e12
+    stage_flops = {"fwd": base, "bwd_main": bwd}
+    dominant = max(per_stage, key=per_stage.get)
+    dom_ms = per_stage[dominant]
+    achieved = stage_flops.get(dominant, 0.0) / (dom_ms * 1e-3) / 1e12
+    traffic = load_traffic(dominant, w.name)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sustained"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sustained"],
+                "traffic": traffic, "kernel": dominant,
+                "peak_kind": f"bf16 dense, sustained ({peaks['source']})",
+                "frac_of_burst_peak": achieved / peaks["bf16"]}
+    fwd_tf = base / (per_stage["fwd"] * 1e-3) / 1e12
+    bwd_ms = per_stage["bwd_prepare"] + per_stage["bwd_main"] + per_stage["bwd_finish"]
+    bwd_tf = bwd / (bwd_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: q, k, v, o, dO take "
+                         f"{5 * q.numel() * 2 / 2**20:.0f} MiB > 129 MB L2; no flush"},
+        "frac_of_peak": value / world / peaks["bf16"],
+        "frac_of_peak_note": f"per-GPU value / {peaks['bf16']} TFLOP/s bf16 dense "
+                             f"({peaks['source']} burst)",
+        "fwd_tflops": fwd_tf, "fwd_frac_of_peak": fwd_tf / peaks["bf16"],
+        "bwd_tflops": bwd_tf,
+        "stage_ms": per_stage,
+        "roofline": roofline,
+        "clocks": clocks,
+        "gpu_launches": args.steps * len(stages),
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_heads)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("fattn", "reference"), default="fattn")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-heads", type=int, default=32)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)      # at least three untimed warm-up steps
+    from exact_attention_fattn_gb300 import workloads as W
+
+    w = W.BY_NAME.get(args.workload)
+    if w is None:
+        name, _, n = args.workload.partition("@N")
+        w = W.BY_NAME[name].with_n(int(n))
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_fattn(args, w)
+
+
+if __name__ == "__main__":
+    main()

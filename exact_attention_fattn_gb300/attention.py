@@ -1,0 +1,156 @@
+"""Python entry points over libfattn, with the C ABI's names.
+
+PyTorch provides device memory and streams only: outputs are allocated as
+torch tensors and their raw pointers, with the current CUDA stream, are
+handed to the library.  Nothing here computes attention.
+"""
+
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib
+
+
+def _stream_ptr(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check_inputs(tensors, d_expected=None):
+    t0 = tensors[0]
+    if not t0.is_cuda:
+        raise ValueError("libfattn works on CUDA tensors; move the inputs to the GPU first")
+    for t in tensors:
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"expected bfloat16 tensors, got {t.dtype}")
+        if t.dim() != 4 or t.shape != t0.shape:
+            raise ValueError("q, k, v (and o, dO) must share one [B, H, N, d] shape")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous [B, H, N, d]")
+        if t.device != t0.device:
+            raise ValueError("tensors must be on one device")
+
+
+def default_scale(d: int) -> float:
+    """1/sqrt(d) ("6.1 FlashAttention V1详解" §1.1), as an fp32 value."""
+    return float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
+
+
+def fattn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None):
+    """Forward pass; returns (O bf16 [B,H,N,d], L fp32 [B,H,N])."""
+    _check_inputs([q, k, v])
+    B, H, N, d = q.shape
+    scale = default_scale(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    lib = _lib.load()
+    with torch.cuda.device(q.device):
+        rc = lib.fattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                           B, H, N, d, int(bool(causal)), scale, _stream_ptr(q.device))
+    _lib.check("fattn_fwd", rc)
+    return o, l
+
+
+def fattn_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(_lib.load().fattn_bwd_workspace_bytes(B, H, N, d))
+
+
+def workspace_for(q) -> torch.Tensor:
+    """A caller-owned uint8 workspace of the size fattn_bwd needs."""
+    B, H, N, d = q.shape
+    nbytes = fattn_bwd_workspace_bytes(B, H, N, d)
+    if nbytes == 0:
+        raise ValueError("unsupported shape")
+    return torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+
+
+def fattn_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
+              workspace=None, dq=None, dk=None, dv=None):
+    """Backward pass; returns (dQ, dK, dV), bf16 [B,H,N,d]."""
+    _check_inputs([q, k, v, o, do])
+    B, H, N, d = q.shape
+    if lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    scale = default_scale(d) if scale is None else float(scale)
+    ws = workspace_for(q) if workspace is None else workspace
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    lib = _lib.load()
+    with torch.cuda.device(q.device):
+        rc = lib.fattn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                           lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                           ws.data_ptr(), ws.numel(), B, H, N, d, int(bool(causal)), scale,
+                           _stream_ptr(q.device))
+    _lib.check("fattn_bwd", rc)
+    return dq, dk, dv
+
+
+def fattn_bwd_prepare(o, do, lse, workspace):
+    _check_inputs([o, do])
+    B, H, N, d = o.shape
+    lib = _lib.load()
+    with torch.cuda.device(o.device):
+        rc = lib.fattn_bwd_prepare(o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                                   workspace.data_ptr(), workspace.numel(), B, H, N, d,
+                                   _stream_ptr(o.device))
+    _lib.check("fattn_bwd_prepare", rc)
+
+
+def fattn_bwd_main(q, k, v, do, workspace, dk, dv, causal: bool = False,
+                   scale: float | None = None):
+    _check_inputs([q, k, v, do, dk, dv])
+    B, H, N, d = q.shape
+    scale = default_scale(d) if scale is None else float(scale)
+    lib = _lib.load()
+    with torch.cuda.device(q.device):
+        rc = lib.fattn_bwd_main(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(),
+                                workspace.data_ptr(), workspace.numel(), dk.data_ptr(),
+                                dv.data_ptr(), B, H, N, d, int(bool(causal)), scale,
+                                _stream_ptr(q.device))
+    _lib.check("fattn_bwd_main", rc)
+
+
+def fattn_bwd_finish(workspace, dq, scale: float | None = None):
+    B, H, N, d = dq.shape
+    scale = default_scale(d) if scale is None else float(scale)
+    lib = _lib.load()
+    with torch.cuda.device(dq.device):
+        rc = lib.fattn_bwd_finish(workspace.data_ptr(), workspace.numel(), dq.data_ptr(),
+                                  B, H, N, d, scale, _stream_ptr(dq.device))
+    _lib.check("fattn_bwd_finish", rc)
+
+
+def fattn_bwd_preprocess(o, do, D, dq_accum):
+    _check_inputs([o, do])
+    B, H, N, d = o.shape
+    lib = _lib.load()
+    with torch.cuda.device(o.device):
+        rc = lib.fattn_bwd_preprocess(o.data_ptr(), do.data_ptr(), D.data_ptr(),
+                                      dq_accum.data_ptr(), B, H, N, d, _stream_ptr(o.device))
+    _lib.check("fattn_bwd_preprocess", rc)
+
+
+def fattn_check_status(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the status."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    lib = _lib.load()
+    with torch.cuda.device(dev):
+        return int(lib.fattn_check_status(_stream_ptr(dev)))
+
+
+def fattn_set_wait_budget(cycles: int) -> None:
+    _lib.load().fattn_set_wait_budget(int(cycles))
+
+
+def fattn_set_rescale_threshold(tau_log2: float) -> None:
+    _lib.load().fattn_set_rescale_threshold(float(tau_log2))
+
+
+def fattn_selftest_timeout(budget_cycles: int, device=None) -> int:
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    lib = _lib.load()
+    with torch.cuda.device(dev):
+        return int(lib.fattn_selftest_timeout(int(budget_cycles), _stream_ptr(dev)))

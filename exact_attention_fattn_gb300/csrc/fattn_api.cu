@@ -1,0 +1,359 @@
+// C-ABI boundary of libfattn: argument validation, tensor-map construction,
+// launch sequencing and the device status word.  See include/fattn.h.
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <mutex>
+
+#include "../../include/fattn.h"
+#include "fattn_internal.h"
+#include "fattn_ptx.cuh"
+
+namespace fattn {
+
+// The single status word of the library on each device.
+__device__ DeviceStatus g_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr long long kDefaultBudget = 1ll << 31;
+
+std::mutex g_mu;
+DeviceStatus* g_status_ptr[kMaxDevices] = {};
+int g_arch_ok[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 unsupported
+long long g_budget = kDefaultBudget;
+float g_tau_log2 = 8.0f;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Per-device setup: architecture check and the status word's address.
+int device_setup(DeviceStatus** status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_arch_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FATTN_ERR_CUDA;
+    g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (g_arch_ok[dev] < 0) return FATTN_ERR_UNSUPPORTED;
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return FATTN_ERR_CUDA;
+    g_status_ptr[dev] = static_cast<DeviceStatus*>(p);
+  }
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return FATTN_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  *status = g_status_ptr[dev];
+  return FATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_sizes(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0) return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  const long long elems = static_cast<long long>(B) * H * N * d;
+  if (elems >= (1ll << 31)) return FATTN_ERR_INVALID_ARG;
+  return FATTN_OK;
+}
+
+bool scale_ok(float s) { return isfinite(s) && s > 0.f; }
+
+// 3-D bf16 view {d, N, B*H} of a [B,H,N,d] tensor, 64-column x box_rows boxes,
+// 128-byte swizzle, zero fill outside the tensor.
+int make_map(CUtensorMap* m, const void* ptr, int N, int BH, int d, int box_rows) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(N) * d * 2};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA; }
+
+}  // namespace
+}  // namespace fattn
+
+using namespace fattn;
+
+extern "C" {
+
+int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int N, int d, int causal, float scale, fattn_stream_t stream) {
+  int rc = check_sizes(B, H, N, d);
+  if (rc != FATTN_OK) return rc;
+  if (!q || !k || !v || !o || !lse) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FATTN_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return FATTN_ERR_INVALID_ARG;
+  DeviceStatus* status = nullptr;
+  if ((rc = device_setup(&status)) != FATTN_OK) return rc;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv, to;
+  if ((rc = make_map(&tq, q, N, BH, d, 128)) != FATTN_OK) return rc;
+  if ((rc = make_map(&tk, k, N, BH, d, 128)) != FATTN_OK) return rc;
+  if ((rc = make_map(&tv, v, N, BH, d, 128)) != FATTN_OK) return rc;
+  if ((rc = make_map(&to, o, N, BH, d, 32)) != FATTN_OK) return rc;
+  FwdArgs a;
+  a.lse = lse;
+  a.status = status;
+  a.N = N;
+  a.BH = BH;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    a.wait_budget = g_budget;
+    a.tau_log2 = g_tau_log2;
+  }
+  return from_cuda(launch_fwd(d, causal != 0, tq, tk, tv, to, a,
+                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// Workspace of the backward pass: D and L*log2(e) in a [B*H, Np] layout
+// (Np = N rounded up to the 128-row tile, so that every tile's 512-byte
+// slice can be fetched by one bulk copy), then the fp32 dQ accumulator.
+}  // extern "C"
+namespace {
+struct BwdWorkspace {
+  size_t d_off, l2_off, acc_off, total;
+  int pitch;
+};
+
+BwdWorkspace bwd_workspace(int B, int H, int N, int d) {
+  BwdWorkspace w;
+  w.pitch = (N + 127) / 128 * 128;
+  const size_t prow = static_cast<size_t>(B) * H * w.pitch;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  w.d_off = 0;
+  w.l2_off = align256(prow * sizeof(float));
+  w.acc_off = w.l2_off + align256(prow * sizeof(float));
+  w.total = w.acc_off + align256(rows * d * sizeof(float));
+  return w;
+}
+}  // namespace
+extern "C" {
+
+size_t fattn_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (check_sizes(B, H, N, d) != FATTN_OK) return 0;
+  return bwd_workspace(B, H, N, d).total;
+}
+
+int fattn_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_accum, int B, int H,
+                         int N, int d, fattn_stream_t stream) {
+  int rc = check_sizes(B, H, N, d);
+  if (rc != FATTN_OK) return rc;
+  if (!o || !dO || !D || !dq_accum) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(D) || !aligned16(dq_accum))
+    return FATTN_ERR_INVALID_ARG;
+  DeviceStatus* status = nullptr;
+  if ((rc = device_setup(&status)) != FATTN_OK) return rc;
+  return from_cuda(launch_bwd_preprocess(o, dO, nullptr, D, nullptr, dq_accum, B * H, N, N, d,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+namespace {
+
+int check_workspace(const void* workspace, size_t workspace_bytes, int B, int H, int N, int d) {
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return FATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < bwd_workspace(B, H, N, d).total) return FATTN_ERR_INVALID_ARG;
+  return FATTN_OK;
+}
+
+int bwd_prepare_impl(const void* o, const void* dO, const float* lse, void* workspace, int B,
+                     int H, int N, int d, cudaStream_t st) {
+  const BwdWorkspace ws = bwd_workspace(B, H, N, d);
+  char* wbase = static_cast<char*>(workspace);
+  return from_cuda(launch_bwd_preprocess(
+      o, dO, lse, reinterpret_cast<float*>(wbase + ws.d_off),
+      reinterpret_cast<float*>(wbase + ws.l2_off), reinterpret_cast<float*>(wbase + ws.acc_off),
+      B * H, N, ws.pitch, d, st));
+}
+
+int bwd_main_impl(const void* q, const void* k, const void* v, const void* dO, void* workspace,
+                  void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
+                  DeviceStatus* status, cudaStream_t st) {
+  const int BH = B * H;
+  const BwdWorkspace ws = bwd_workspace(B, H, N, d);
+  char* wbase = static_cast<char*>(workspace);
+  int rc;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  if ((rc = make_map(&tq, q, N, BH, d, 128)) != FATTN_OK) return rc;
+  if ((rc = make_map(&tk, k, N, BH, d, 128)) != FATTN_OK) return rc;
+  if ((rc = make_map(&tv, v, N, BH, d, 128)) != FATTN_OK) return rc;
+  if ((rc = make_map(&tdo, dO, N, BH, d, 128)) != FATTN_OK) return rc;
+  if ((rc = make_map(&tdk, dk, N, BH, d, 32)) != FATTN_OK) return rc;
+  if ((rc = make_map(&tdv, dv, N, BH, d, 32)) != FATTN_OK) return rc;
+  BwdArgs a;
+  a.L2 = reinterpret_cast<const float*>(wbase + ws.l2_off);
+  a.D = reinterpret_cast<const float*>(wbase + ws.d_off);
+  a.dq_accum = reinterpret_cast<float*>(wbase + ws.acc_off);
+  a.status = status;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    a.wait_budget = g_budget;
+  }
+  a.N = N;
+  a.BH = BH;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  return from_cuda(launch_bwd_main(d, causal != 0, tq, tk, tv, tdo, tdk, tdv, a, st));
+}
+
+int bwd_finish_impl(const void* workspace, void* dq, int B, int H, int N, int d, float scale,
+                    cudaStream_t st) {
+  const BwdWorkspace ws = bwd_workspace(B, H, N, d);
+  const float* acc =
+      reinterpret_cast<const float*>(static_cast<const char*>(workspace) + ws.acc_off);
+  return from_cuda(
+      launch_dq_convert(acc, dq, static_cast<long long>(B) * H * N * d, scale, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+int fattn_bwd_prepare(const void* o, const void* dO, const float* lse, void* workspace,
+                      size_t workspace_bytes, int B, int H, int N, int d,
+                      fattn_stream_t stream) {
+  int rc = check_sizes(B, H, N, d);
+  if (rc != FATTN_OK) return rc;
+  if (!o || !dO || !lse) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(lse)) return FATTN_ERR_INVALID_ARG;
+  if ((rc = check_workspace(workspace, workspace_bytes, B, H, N, d)) != FATTN_OK) return rc;
+  DeviceStatus* status = nullptr;
+  if ((rc = device_setup(&status)) != FATTN_OK) return rc;
+  return bwd_prepare_impl(o, dO, lse, workspace, B, H, N, d,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fattn_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* workspace,
+                   size_t workspace_bytes, void* dk, void* dv, int B, int H, int N, int d,
+                   int causal, float scale, fattn_stream_t stream) {
+  int rc = check_sizes(B, H, N, d);
+  if (rc != FATTN_OK) return rc;
+  if (!q || !k || !v || !dO || !dk || !dv) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dk) ||
+      !aligned16(dv))
+    return FATTN_ERR_INVALID_ARG;
+  if ((rc = check_workspace(workspace, workspace_bytes, B, H, N, d)) != FATTN_OK) return rc;
+  if (!scale_ok(scale)) return FATTN_ERR_INVALID_ARG;
+  DeviceStatus* status = nullptr;
+  if ((rc = device_setup(&status)) != FATTN_OK) return rc;
+  return bwd_main_impl(q, k, v, dO, workspace, dk, dv, B, H, N, d, causal, scale, status,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fattn_bwd_finish(const void* workspace, size_t workspace_bytes, void* dq, int B, int H, int N,
+                     int d, float scale, fattn_stream_t stream) {
+  int rc = check_sizes(B, H, N, d);
+  if (rc != FATTN_OK) return rc;
+  if (!dq || !aligned16(dq)) return FATTN_ERR_INVALID_ARG;
+  if ((rc = check_workspace(workspace, workspace_bytes, B, H, N, d)) != FATTN_OK) return rc;
+  if (!scale_ok(scale)) return FATTN_ERR_INVALID_ARG;
+  DeviceStatus* status = nullptr;
+  if ((rc = device_setup(&status)) != FATTN_OK) return rc;
+  return bwd_finish_impl(workspace, dq, B, H, N, d, scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fattn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+              const float* lse, void* dq, void* dk, void* dv, void* workspace,
+              size_t workspace_bytes, int B, int H, int N, int d, int causal, float scale,
+              fattn_stream_t stream) {
+  int rc = check_sizes(B, H, N, d);
+  if (rc != FATTN_OK) return rc;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FATTN_ERR_INVALID_ARG;
+  if ((rc = check_workspace(workspace, workspace_bytes, B, H, N, d)) != FATTN_OK) return rc;
+  if (!scale_ok(scale)) return FATTN_ERR_INVALID_ARG;
+  DeviceStatus* status = nullptr;
+  if ((rc = device_setup(&status)) != FATTN_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = bwd_prepare_impl(o, dO, lse, workspace, B, H, N, d, st)) != FATTN_OK) return rc;
+  if ((rc = bwd_main_impl(q, k, v, dO, workspace, dk, dv, B, H, N, d, causal, scale, status,
+                          st)) != FATTN_OK)
+    return rc;
+  return bwd_finish_impl(workspace, dq, B, H, N, d, scale, st);
+}
+
+int fattn_check_status(fattn_stream_t stream) {
+  DeviceStatus* status = nullptr;
+  int rc = device_setup(&status);
+  if (rc != FATTN_OK) return rc;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return FATTN_ERR_CUDA;
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return FATTN_ERR_CUDA;
+  DeviceStatus host = {};
+  if (cudaMemcpyFromSymbol(&host, g_status, sizeof(host)) != cudaSuccess) return FATTN_ERR_CUDA;
+  if (host.code != 0) {
+    DeviceStatus zero = {};
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess) return FATTN_ERR_CUDA;
+    return static_cast<int>(host.code);
+  }
+  return FATTN_OK;
+}
+
+const char* fattn_status_string(int status) {
+  switch (status) {
+    case FATTN_OK: return "ok";
+    case FATTN_ERR_INVALID_ARG: return "invalid argument";
+    case FATTN_ERR_UNSUPPORTED: return "unsupported head dimension or device";
+    case FATTN_ERR_CUDA: return "CUDA error";
+    case FATTN_ERR_TIMEOUT: return "kernel wait timed out";
+    default: return "unknown status";
+  }
+}
+
+void fattn_set_wait_budget(long long cycles) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_budget = cycles > 0 ? cycles : kDefaultBudget;
+}
+
+void fattn_set_rescale_threshold(float tau_log2) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!(tau_log2 >= 0.f)) tau_log2 = 8.0f;
+  g_tau_log2 = tau_log2 > 16.f ? 16.f : tau_log2;
+}
+
+int fattn_selftest_timeout(long long budget_cycles, fattn_stream_t stream) {
+  DeviceStatus* status = nullptr;
+  int rc = device_setup(&status);
+  if (rc != FATTN_OK) return rc;
+  if (budget_cycles <= 0) return FATTN_ERR_INVALID_ARG;
+  return from_cuda(
+      launch_selftest_timeout(status, budget_cycles, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* fattn_version(void) { return "0.1.0"; }
+
+}  // extern "C"

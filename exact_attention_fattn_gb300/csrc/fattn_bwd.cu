@@ -1,0 +1,453 @@
+// Main backward kernel of exact attention on sm_103a.
+//
+// Recomputation backward ("6.1 FlashAttention V1详解" §6.1-6.2): one CTA owns
+// a 128-row K/V tile j of one (batch, head) and walks the 128-row Q tiles i
+// (i >= j when causal).  Per step, with the kv rows on TMEM lanes:
+//   S^T  = K_j Q_i^T                    (tcgen05, fp32 in TMEM)
+//   P^T  = 2^(S^T*scale*log2e - L_i*log2e)    (one thread per kv row; bf16 back to TMEM)
+//   dP^T = V_j dO_i^T                   (tcgen05)
+//   dS^T = P^T o (dP^T - D_i)           (bf16 to TMEM and, as dS, to shared memory)
+//   dV_j += P^T dO_i,  dK_j += dS^T Q_i (tcgen05, accumulators in TMEM)
+//   dQ_i  = dS K_j                      (tcgen05) -> fp32 atomics into dq_accum
+// At the end dK_j * scale and dV_j are stored as bf16.  dQ = scale * dq_accum
+// is converted by a separate kernel.  The dQ and dK formulas follow from
+// S = scale Q K^T by the chain rule (the pages stop at dS).
+//
+// Warps: 0-3 compute (TMEM lanes 0..127), 4 TMEM allocation + MMA issue,
+// 5 TMA producer.
+// TMEM (512 columns): A [0,128) holds S^T, then P^T (bf16, [0,64)), then dQ
+// ([0,d)); B [128,256) holds dP^T, then dS^T (bf16, [128,192)); dV at
+// [256,256+d), dK at [256+d,256+2d).
+#include "fattn_internal.h"
+#include "fattn_ptx.cuh"
+
+namespace fattn {
+
+namespace {
+
+constexpr int kTile = 128;     // rows per Q tile and per K/V tile
+constexpr int kThreads = 192;
+constexpr int kMmaWarp = 4;
+constexpr int kLoadWarp = 5;
+constexpr uint32_t kColA = 0, kColB = 128, kColDV = 256;
+
+template <int HD>
+struct BwdCfg {
+  static constexpr int kChunks = HD / 64;
+  static constexpr int kChunkBytes = kTile * 128;   // 128 rows x 128 bytes
+  static constexpr int kTileBytes = kTile * HD * 2;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kTileBytes;
+  static constexpr int kStageOff = 2 * kTileBytes;  // stage s: Q_i then dO_i
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kDsOff = kStageOff + 2 * kStageBytes;
+  static constexpr int kDsBytes = kTile * kTile * 2;
+  static constexpr int kLdOff = kDsOff + kDsBytes;  // stage s: L2[128], D[128]
+  static constexpr int kBarOff = kLdOff + 2 * 1024;
+  static constexpr int kNumBars = 13;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16;
+  static constexpr uint32_t kColDK = kColDV + HD;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+// Barrier indices.
+enum : int {
+  kBarKv = 0,
+  kBarQFull = 1,   // +stage
+  kBarQEmpty = 3,  // +stage
+  kBarSFull = 5,
+  kBarDpFull = 6,
+  kBarPFull = 7,
+  kBarDsFull = 8,
+  kBarDqFull = 9,
+  kBarDqEmpty = 10,
+  kBarDkvFull = 11,
+  kBarMmaDone = 12,
+};
+
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+template <int HD, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+               const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+               const BwdArgs args) {
+  using C = BwdCfg<HD>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  // The 128-byte swizzle needs 1024-byte aligned tiles.  The budget leaves no
+  // room to realign, so a misaligned base is reported instead of used.
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0 && atomicCAS(&args.status->code, 0u, 2u) == 0u) args.status->where = 100;
+    return;
+  }
+  auto bar = [&](int i) { return sbase + C::kBarOff + 8u * i; };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int N = args.N;
+  const int n_tiles = (N + kTile - 1) / kTile;
+  const int pitch = n_tiles * kTile;
+  const int bh = blockIdx.x % args.BH;
+  const int j = blockIdx.x / args.BH;      // K/V tile; small j has the most Q tiles
+  const int kv0 = j * kTile;
+  const int i0 = CAUSAL ? j : 0;
+  const int n_it = n_tiles - i0;           // >= 1
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kBarKv), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kBarQFull + s), 1);
+      mbar_init(bar(kBarQEmpty + s), 1);
+    }
+    mbar_init(bar(kBarSFull), 1);
+    mbar_init(bar(kBarDpFull), 1);
+    mbar_init(bar(kBarPFull), 128);
+    mbar_init(bar(kBarDsFull), 128);
+    mbar_init(bar(kBarDqFull), 1);
+    mbar_init(bar(kBarDqEmpty), 128);
+    mbar_init(bar(kBarDkvFull), 1);
+    mbar_init(bar(kBarMmaDone), 1);
+    misc[1] = 0u;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&misc[0]), 512);
+    tmem_relinquish();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dk);
+    tma_prefetch_desc(&tm_dv);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const WaitCtx wc{args.wait_budget, reinterpret_cast<volatile uint32_t*>(&misc[1]), args.status};
+
+  if (warp < 4) {
+    // ================================================================ compute
+    const int r = warp * 32 + lane;          // kv row of the tile = TMEM lane
+    const int kv = kv0 + r;
+    const bool kv_valid = kv < N;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tA = tmem + lane_off + kColA;
+    const uint32_t tB = tmem + lane_off + kColB;
+    const float c = args.scale_log2;
+    const uint32_t ds_base = sbase + C::kDsOff;
+    const uint32_t stg = ds_base + warp * 8192;  // per-warp staging for dQ rows
+    bool ok = true;
+    for (int it = 0; it < n_it && ok; ++it) {
+      const int i = i0 + it;
+      const int q0 = i * kTile;
+      const int s = it & 1;
+      const uint32_t ph = it & 1;
+      const float* l2s = reinterpret_cast<const float*>(smem + C::kLdOff + s * 1024);
+      const float* ds_vec = l2s + 128;
+      // ---- P^T = 2^(S^T c - L2) (masked)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull), ph, wc, kWaitSFull));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t p0[32], p1[32], p2[32], p3[32];
+      tmem_ld32(tA + 0, p0);
+      tmem_ld32(tA + 32, p1);
+      tmem_ld32(tA + 64, p2);
+      tmem_ld32(tA + 96, p3);
+      tmem_ld_wait32(p0);
+      reg_fence32(p1);
+      reg_fence32(p2);
+      reg_fence32(p3);
+      uint32_t* pv[4] = {p0, p1, p2, p3};
+      const bool diag = CAUSAL && q0 == kv0;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(l2s + g * 32 + e);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int col = g * 32 + e + u;
+            float p = ex2_approx(fmaf(__uint_as_float(pv[g][e + u]), c, -lv[u]));
+            if (!kv_valid || (diag && col < r)) p = 0.f;
+            pv[g][e + u] = __float_as_uint(p);
+          }
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(pv[g][2 * e]), __uint_as_float(pv[g][2 * e + 1]));
+        tmem_st16(tA + 16 * g, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(kBarPFull));
+      // ---- dS^T = P^T o (dP^T - D)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDpFull), ph, wc, kWaitDpFull));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint32_t dp[32];
+        tmem_ld32(tB + 32 * g, dp);
+        tmem_ld_wait32(dp);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(ds_vec + g * 32 + e);
+          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          float dsv[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            dsv[u] = __uint_as_float(pv[g][e + u]) * (__uint_as_float(dp[e + u]) - dv4[u]);
+          pk[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
+          pk[e / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+        }
+        tmem_st16(tB + 16 * g, pk);
+        // dS row r, q columns [32g, 32g+32) = four 16-byte chunks of the
+        // MN-major (q contiguous) operand: two 64-column atoms, 128-byte
+        // swizzle inside each.
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          const int c16 = g * 4 + qq;
+          const uint32_t addr = ds_base + (c16 >> 3) * 16384 + r * 128 +
+                                (static_cast<uint32_t>((c16 & 7) ^ (r & 7)) << 4);
+          st_shared_v4(addr, pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(kBarDsFull));
+      // ---- dQ_i rows (TMEM lane = q row) -> fp32 atomics, through a
+      // per-warp shared-memory transpose so that each atomic instruction
+      // covers four 128-byte row segments.
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDqFull), ph, wc, kWaitDqFull));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int ch = 0; ch < HD / 32; ++ch) {
+        uint32_t dq[32];
+        tmem_ld32(tA + 32 * ch, dq);
+        tmem_ld_wait32(dq);
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4)
+          st_shared_v4(stg + lane * 128 + (static_cast<uint32_t>(c4 ^ (lane & 7)) << 4),
+                       dq[4 * c4], dq[4 * c4 + 1], dq[4 * c4 + 2], dq[4 * c4 + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int k4 = 0; k4 < 8; ++k4) {
+          const int rl = k4 * 4 + (lane >> 3);
+          const int c4 = lane & 7;
+          const float4 v = *reinterpret_cast<const float4*>(
+              smem + C::kDsOff + warp * 8192 + rl * 128 + ((c4 ^ (rl & 7)) << 4));
+          const int q = q0 + warp * 32 + rl;
+          if (q < N)
+            atomicAdd(reinterpret_cast<float4*>(
+                          args.dq_accum + (static_cast<size_t>(bh) * N + q) * HD + ch * 32 + c4 * 4),
+                      v);
+        }
+        __syncwarp();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(kBarDqEmpty));
+    }
+    // ---- epilogue: dV_j, dK_j * scale -> bf16 -> K/V shared memory -> TMA
+    if (ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDkvFull), 0, wc, kWaitOFull));
+      if (ok) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t tsrc = tmem + lane_off + (which == 0 ? kColDV : C::kColDK);
+          const float mul = which == 0 ? 1.f : args.scale;
+          const uint32_t stage = sbase + (which == 0 ? C::kVOff : C::kKOff);
+#pragma unroll 1
+          for (int ch = 0; ch < HD / 32; ++ch) {
+            uint32_t o[32];
+            tmem_ld32(tsrc + 32 * ch, o);
+            tmem_ld_wait32(o);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * mul,
+                                  __uint_as_float(o[2 * e + 1]) * mul);
+            const uint32_t rowaddr = stage + (ch >> 1) * C::kChunkBytes + r * 128;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              const uint32_t chunk = (ch & 1) * 4 + qq;
+              st_shared_v4(rowaddr + ((chunk ^ (r & 7)) << 4), pk[4 * qq], pk[4 * qq + 1],
+                           pk[4 * qq + 2], pk[4 * qq + 3]);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && kv0 + warp * 32 < N) {
+#pragma unroll
+          for (int cc = 0; cc < C::kChunks; ++cc) {
+            tma_store_3d(&tm_dv, sbase + C::kVOff + cc * C::kChunkBytes + warp * 32 * 128,
+                         cc * 64, kv0 + warp * 32, bh);
+            tma_store_3d(&tm_dk, sbase + C::kKOff + cc * C::kChunkBytes + warp * 32 * 128,
+                         cc * 64, kv0 + warp * 32, bh);
+          }
+          bulk_commit_group();
+          bulk_wait_group_read0();
+        }
+        __syncwarp();
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ================================================================ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc_kk = idesc_bf16_f32(kTile, kTile, false, false);
+      constexpr uint32_t idesc_tm = idesc_bf16_f32(kTile, HD, false, true);
+      constexpr uint32_t idesc_mm = idesc_bf16_f32(kTile, HD, true, true);
+      const uint32_t sK = sbase + C::kKOff, sV = sbase + C::kVOff, sDs = sbase + C::kDsOff;
+      auto sQ = [&](int s) { return sbase + C::kStageOff + s * C::kStageBytes; };
+      auto sDo = [&](int s) { return sbase + C::kStageOff + s * C::kStageBytes + C::kTileBytes; };
+      // D(128 x 128) = A(128 x HD) B(128 x HD)^T, both K-major (HD contiguous).
+      auto mma_kmajor = [&](uint32_t d, uint32_t a, uint32_t b) {
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+          mma_ss(d, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), idesc_kk,
+                 kk > 0 ? 1u : 0u);
+        }
+      };
+      // D(128 x HD) (+)= A(tmem, 128 x 128) B, B MN-major (HD contiguous).
+      auto mma_tmem_a = [&](uint32_t d, uint32_t a_col, uint32_t b, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(d, tmem + a_col + 8 * kk, sdesc_sw128(b + kk * 2048, C::kChunkBytes, 1024),
+                 idesc_tm, (acc || kk > 0) ? 1u : 0u);
+      };
+      auto qfull = [&](int it) {
+        return mbar_wait(bar(kBarQFull + (it & 1)), (it >> 1) & 1, wc, kWaitKvFull);
+      };
+      if (!mbar_wait(bar(kBarKv), 0, wc, kWaitKvFull)) goto mma_end;
+      if (!qfull(0)) goto mma_end;
+      tc_fence_after();
+      mma_kmajor(tmem + kColA, sK, sQ(0));   // S^T
+      mma_commit(bar(kBarSFull));
+      mma_kmajor(tmem + kColB, sV, sDo(0));  // dP^T
+      mma_commit(bar(kBarDpFull));
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it & 1;
+        const uint32_t ph = it & 1;
+        if (!mbar_wait(bar(kBarPFull), ph, wc, kWaitPFull)) goto mma_end;
+        tc_fence_after();
+        mma_tmem_a(tmem + kColDV, kColA, sDo(s), it > 0);       // dV += P^T dO
+        if (!mbar_wait(bar(kBarDsFull), ph, wc, kWaitDsFull)) goto mma_end;
+        tc_fence_after();
+        mma_tmem_a(tmem + C::kColDK, kColB, sQ(s), it > 0);     // dK += dS^T Q
+        // dQ = dS K: A = dS (q contiguous, MN-major), B = K (HD contiguous).
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ss(tmem + kColA, sdesc_sw128(sDs + kk * 2048, 16384, 1024),
+                 sdesc_sw128(sK + kk * 2048, C::kChunkBytes, 1024), idesc_mm,
+                 kk > 0 ? 1u : 0u);
+        mma_commit(bar(kBarDqFull));
+        mma_commit(bar(kBarQEmpty + s));
+        if (it + 1 < n_it) {
+          if (!qfull(it + 1)) goto mma_end;
+          tc_fence_after();
+          mma_kmajor(tmem + kColB, sV, sDo(s ^ 1));             // dP^T (next)
+          mma_commit(bar(kBarDpFull));
+          if (!mbar_wait(bar(kBarDqEmpty), ph, wc, kWaitDqEmpty)) goto mma_end;
+          tc_fence_after();
+          mma_kmajor(tmem + kColA, sK, sQ(s ^ 1));              // S^T (next)
+          mma_commit(bar(kBarSFull));
+        }
+      }
+      mma_commit(bar(kBarDkvFull));
+    mma_end:
+      mma_commit(bar(kBarMmaDone));
+      mbar_wait_drain(bar(kBarMmaDone), 0, args.wait_budget);
+    }
+    __syncwarp();
+  } else if (warp == kLoadWarp) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(kBarKv), 2 * C::kTileBytes);
+      for (int cc = 0; cc < C::kChunks; ++cc) {
+        tma_load_3d(sbase + C::kKOff + cc * C::kChunkBytes, &tm_k, bar(kBarKv), cc * 64, kv0, bh);
+        tma_load_3d(sbase + C::kVOff + cc * C::kChunkBytes, &tm_v, bar(kBarKv), cc * 64, kv0, bh);
+      }
+      int issued = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it & 1;
+        const int rnd = it >> 1;
+        if (rnd > 0 && !mbar_wait(bar(kBarQEmpty + s), (rnd - 1) & 1, wc, kWaitKvEmpty)) break;
+        const uint32_t full = bar(kBarQFull + s);
+        mbar_arrive_expect_tx(full, 2 * C::kTileBytes + 1024);
+        const int q0 = (i0 + it) * kTile;
+        const uint32_t dst = sbase + C::kStageOff + s * C::kStageBytes;
+        for (int cc = 0; cc < C::kChunks; ++cc) {
+          tma_load_3d(dst + cc * C::kChunkBytes, &tm_q, full, cc * 64, q0, bh);
+          tma_load_3d(dst + C::kTileBytes + cc * C::kChunkBytes, &tm_do, full, cc * 64, q0, bh);
+        }
+        const size_t vec = static_cast<size_t>(bh) * pitch + q0;
+        bulk_load_1d(sbase + C::kLdOff + s * 1024, args.L2 + vec, 512, full);
+        bulk_load_1d(sbase + C::kLdOff + s * 1024 + 512, args.D + vec, 512, full);
+        issued = it + 1;
+      }
+      for (int it = max(0, issued - 2); it < issued; ++it)
+        mbar_wait_drain(bar(kBarQFull + (it & 1)), (it >> 1) & 1, args.wait_budget);
+      mbar_wait_drain(bar(kBarKv), 0, args.wait_budget);
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int HD, bool CAUSAL>
+cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                         const BwdArgs& a, cudaStream_t stream) {
+  using C = BwdCfg<HD>;
+  auto kern = bwd_kernel<HD, CAUSAL>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int n_tiles = (a.N + kTile - 1) / kTile;
+  const dim3 grid(static_cast<unsigned>(n_tiles * a.BH));
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdk, tdv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_main(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo,
+                            const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdArgs& a,
+                            cudaStream_t stream) {
+  if (d == 64) {
+    return causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, tdk, tdv, a, stream)
+                  : launch_bwd_t<64, false>(tq, tk, tv, tdo, tdk, tdv, a, stream);
+  }
+  return causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, tdk, tdv, a, stream)
+                : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdk, tdv, a, stream);
+}
+
+}  // namespace fattn

@@ -1,0 +1,59 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fattn {
+
+struct DeviceStatus;
+
+// Everything a forward launch needs besides the tensor maps.
+struct FwdArgs {
+  float* lse;                 // [BH, N]
+  DeviceStatus* status;
+  long long wait_budget;      // cycles
+  int N;
+  int BH;
+  float scale_log2;           // scale * log2(e)
+  float tau_log2;             // rescale threshold (log2 units)
+};
+
+// Launch the forward kernel for head dim d (64/128).  Tensor maps are 3-D
+// {d, N, B*H} views with a 128-byte swizzle: q/k/v with 128-row boxes, o with
+// 32-row boxes.
+cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a,
+                       cudaStream_t stream);
+
+struct BwdArgs {
+  const float* L2;            // [BH, Np]: lse * log2(e), +inf past N (Np = N rounded up to 128)
+  const float* D;             // [BH, Np]: rowsum(dO o O), 0 past N
+  float* dq_accum;            // [BH, N, d] fp32
+  DeviceStatus* status;
+  long long wait_budget;
+  int N;
+  int BH;
+  float scale;
+  float scale_log2;
+};
+
+// D (and, when L2 != nullptr, L2 = lse * log2 e) in a [BH, pitch] layout with
+// padding rows N..pitch-1; zeroes dq_accum [BH, N, d].
+cudaError_t launch_bwd_preprocess(const void* o, const void* dO, const float* lse, float* D,
+                                  float* L2, float* dq_accum, int BH, int N, int pitch, int d,
+                                  cudaStream_t stream);
+
+cudaError_t launch_bwd_main(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo,
+                            const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdArgs& a,
+                            cudaStream_t stream);
+
+cudaError_t launch_dq_convert(const float* dq_accum, void* dq, long long elems, float scale,
+                              cudaStream_t stream);
+
+cudaError_t launch_selftest_timeout(DeviceStatus* status, long long budget, cudaStream_t stream);
+
+}  // namespace fattn

@@ -1,0 +1,169 @@
+/*
+ * libfattn — exact, IO-aware scaled-dot-product attention for GB300 (sm_103a).
+ *
+ * The problem follows the pages' statement of it ("6.1 FlashAttention V1详解",
+ * §8.1 tensor shapes): Q, K, V are [B, H, N, d] (batch, head, sequence,
+ * head dimension); the forward pass writes O [B, H, N, d] and a per-row
+ * logsumexp L [B, H, N]; the backward pass recomputes P from Q, K and L and
+ * writes dQ, dK, dV.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  Tensors are
+ *    dense and contiguous: bf16 [B, H, N, d] for q, k, v, o, dO, dq, dk, dv;
+ *    fp32 [B, H, N] for lse.  Every pointer must be 16-byte aligned.
+ *  - d is 64 or 128.  B, H, N >= 1 and B*H*N*d < 2^31.  Self-attention only
+ *    (the key length equals the query length N).
+ *  - scale multiplies Q K^T; it must be finite and > 0 (the usual choice is
+ *    1/sqrt(d), "6.1 FlashAttention V1详解" §1.1).
+ *  - causal != 0 hides key j from query i when j > i (square, top-left
+ *    aligned mask).
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream) and
+ *    return once the work is enqueued.  The library allocates no memory per
+ *    call; the backward pass takes a caller-owned workspace.
+ *  - Errors: argument problems return FATTN_ERR_INVALID_ARG or
+ *    FATTN_ERR_UNSUPPORTED and enqueue nothing.  A failed launch returns
+ *    FATTN_ERR_CUDA.  Kernels never trap: a pipeline wait that exceeds its
+ *    time budget makes the kernel record FATTN_ERR_TIMEOUT in a device status
+ *    word and return; fattn_check_status() reports (and clears) it.
+ */
+#ifndef FATTN_H_
+#define FATTN_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fattn_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  FATTN_OK = 0,
+  FATTN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or scale */
+  FATTN_ERR_UNSUPPORTED = 2, /* d not in {64,128}, or the device is not sm_103 */
+  FATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+  FATTN_ERR_TIMEOUT = 4      /* a kernel gave up on a pipeline wait */
+} fattn_status;
+
+/*
+ * Forward pass.
+ * Computes S = scale * Q K^T (masked), P = softmax(S) row-wise, O = P V, and
+ * L = m + log(l) per row (natural log) — "6.1 FlashAttention V1详解" §1.1 and
+ * §3.2 (online softmax), "FlashAttention v1～v4" v2 §1 (L instead of m, l).
+ * The N x N matrices S and P never reach device memory.
+ *   q, k, v : in,  bf16 [B,H,N,d]
+ *   o       : out, bf16 [B,H,N,d]
+ *   lse     : out, fp32 [B,H,N]
+ * Returns a fattn_status.
+ */
+int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+              int B, int H, int N, int d, int causal, float scale,
+              fattn_stream_t stream);
+
+/*
+ * Backward preprocessing: D_i = sum_k dO_ik * O_ik (fp32, one value per row;
+ * the identity rowsum(dP o P) = rowsum(dO o O) of "6.1 FlashAttention
+ * V1详解" §6.1), and zero the fp32 dQ accumulator.
+ *   o, dO    : in,  bf16 [B,H,N,d]
+ *   D        : out, fp32 [B,H,N]
+ *   dq_accum : out, fp32 [B,H,N,d], set to zero
+ * fattn_bwd runs this itself; it is exported for callers that schedule it.
+ */
+int fattn_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_accum,
+                         int B, int H, int N, int d, fattn_stream_t stream);
+
+/*
+ * Workspace the backward pass needs, in bytes: D and L*log2(e) (fp32, each
+ * [B*H, Np] with Np = N rounded up to a multiple of 128), then the fp32 dQ
+ * accumulator ([B,H,N,d]); each part starts on a 256-byte boundary.
+ * Returns 0 for invalid sizes.
+ */
+size_t fattn_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward pass ("6.1 FlashAttention V1详解" §6.1-6.2, recomputation):
+ * P is rebuilt from Q, K and L; then dV = P^T dO, dP = dO V^T,
+ * dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q (the last two by
+ * the chain rule through S = scale Q K^T).
+ *   q, k, v, o, dO : in,  bf16 [B,H,N,d];  lse: in, fp32 [B,H,N] from fattn_fwd
+ *   dq, dk, dv     : out, bf16 [B,H,N,d]
+ *   workspace      : scratch of at least fattn_bwd_workspace_bytes(B,H,N,d),
+ *                    256-byte aligned, caller-owned; contents on entry ignored
+ * Enqueues, in order: preprocess, the main backward kernel (dQ accumulated
+ * with fp32 atomics), and the dQ conversion.  Returns a fattn_status.
+ */
+int fattn_bwd(const void* q, const void* k, const void* v, const void* o,
+              const void* dO, const float* lse, void* dq, void* dk, void* dv,
+              void* workspace, size_t workspace_bytes,
+              int B, int H, int N, int d, int causal, float scale,
+              fattn_stream_t stream);
+
+/*
+ * The three stages that fattn_bwd enqueues, exported for callers that time
+ * or schedule them separately.  Run in this order on one workspace they do
+ * exactly what fattn_bwd does:
+ *   fattn_bwd_prepare: D = rowsum(dO o O) and L*log2(e) into the workspace,
+ *                      and zero its fp32 dQ accumulator;
+ *   fattn_bwd_main:    the recomputation kernel: writes dk, dv and adds the
+ *                      dQ partial sums into the accumulator;
+ *   fattn_bwd_finish:  dq = bf16(scale * accumulator).
+ * Arguments have the meaning given for fattn_bwd; the workspace must hold at
+ * least fattn_bwd_workspace_bytes(B,H,N,d) bytes, 256-byte aligned.
+ */
+int fattn_bwd_prepare(const void* o, const void* dO, const float* lse,
+                      void* workspace, size_t workspace_bytes,
+                      int B, int H, int N, int d, fattn_stream_t stream);
+int fattn_bwd_main(const void* q, const void* k, const void* v, const void* dO,
+                   void* workspace, size_t workspace_bytes, void* dk, void* dv,
+                   int B, int H, int N, int d, int causal, float scale,
+                   fattn_stream_t stream);
+int fattn_bwd_finish(const void* workspace, size_t workspace_bytes, void* dq,
+                     int B, int H, int N, int d, float scale, fattn_stream_t stream);
+
+/*
+ * Synchronise `stream`, then report the first error since the last call:
+ * a pending asynchronous CUDA error (FATTN_ERR_CUDA) or a kernel wait
+ * timeout recorded on the current device (FATTN_ERR_TIMEOUT).  Clears the
+ * device status word.  Returns FATTN_OK when neither happened.
+ */
+int fattn_check_status(fattn_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* fattn_status_string(int status);
+
+/*
+ * Budget, in SM clock cycles, for every pipeline wait inside the kernels
+ * (default 2^31, about one second).  Values <= 0 restore the default.
+ * Applies to launches made after the call, from any thread.
+ */
+void fattn_set_wait_budget(long long cycles);
+
+/*
+ * Threshold, in log2 units, of the conditional rescaling in the forward pass
+ * ("FlashAttention v1～v4" v4 §3): the reference max of a row moves only when
+ * the row max exceeds it by more than tau_log2, and O, l are rescaled only
+ * then.  The result is exact for any tau_log2 >= 0 because l and O always
+ * share the reference; probabilities stay <= 2^tau_log2.  Default 8
+ * (log2 256, the page's value).  Negative values restore the default;
+ * values above 16 are clamped to 16.  Applies to later launches.
+ */
+void fattn_set_rescale_threshold(float tau_log2);
+
+/*
+ * Self-test of the timeout path: launches one block that waits, with the
+ * given cycle budget, on a barrier that nothing ever completes.  The wait
+ * gives up, records FATTN_ERR_TIMEOUT in the status word and the kernel
+ * returns; the next fattn_check_status() reports it.  Returns FATTN_OK if
+ * the launch was enqueued.
+ */
+int fattn_selftest_timeout(long long budget_cycles, fattn_stream_t stream);
+
+/* Library version, "major.minor.patch". */
+const char* fattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FATTN_H_ */

@@ -1,0 +1,149 @@
+"""Backward parity: libfattn on the GPU vs the fp64 oracle's analytic
+gradients on the same inputs."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_fattn_gb300 import attention as A
+from exact_attention_fattn_gb300 import workloads as W
+from gpu_util import gather_rows, run_fwd, to_np
+from tolerances import check_grad
+
+pytestmark = pytest.mark.gpu
+
+
+def run_fwd_bwd(inp, causal, scale):
+    o, lse = run_fwd(inp, causal, scale)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    dq, dk, dv = A.fattn_bwd(q, k, v, o, do, lse, causal=causal, scale=scale)
+    status = A.fattn_check_status()
+    assert status == 0, f"fattn status {status}"
+    return dq, dk, dv
+
+
+SMALL = [
+    (1, 1, 128, 64, False),
+    (1, 2, 200, 64, True),
+    (2, 1, 1, 128, False),
+    (1, 1, 1, 64, True),
+    (1, 2, 129, 128, True),
+    (1, 1, 257, 128, False),
+    (2, 2, 333, 64, True),
+    (1, 2, 640, 128, True),
+    (1, 2, 1000, 128, False),
+    (1, 1, 511, 64, False),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", SMALL)
+def test_bwd_small(B, H, N, d, causal):
+    w = W.Workload("case", B, H, N, d, causal, seed=31 + N + d)
+    inp = W.make_inputs(w)
+    dq, dk, dv = run_fwd_bwd(inp, causal, w.scale)
+    gq, gk, gv, _ = oracle.attention_backward(inp["q"], inp["k"], inp["v"], inp["do"], causal,
+                                              w.scale)
+    check_grad(to_np(dq), gq, "dQ")
+    check_grad(to_np(dk), gk, "dK")
+    check_grad(to_np(dv), gv, "dV")
+
+
+def test_bwd_outlier_rows_small():
+    """Large-score rows (x20) as in the causal benchmark workload, at a size
+    the oracle evaluates in full."""
+    w = W.Workload("outl", 1, 2, 768, 128, True, outlier_frac=0.01, outlier_mult=20.0, seed=77)
+    inp = W.make_inputs(w)
+    dq, dk, dv = run_fwd_bwd(inp, True, w.scale)
+    gq, gk, gv, _ = oracle.attention_backward(inp["q"], inp["k"], inp["v"], inp["do"], True,
+                                              w.scale)
+    check_grad(to_np(dq), gq, "dQ")
+    check_grad(to_np(dk), gk, "dK")
+    check_grad(to_np(dv), gv, "dV")
+
+
+def test_bwd_medium_d64_full():
+    w = W.MEDIUM_D64
+    inp = W.make_inputs(w)
+    dq, dk, dv = run_fwd_bwd(inp, w.causal, w.scale)
+    gq, gk, gv, _ = oracle.attention_backward(inp["q"], inp["k"], inp["v"], inp["do"], w.causal,
+                                              w.scale)
+    check_grad(to_np(dq), gq, "dQ")
+    check_grad(to_np(dk), gk, "dK")
+    check_grad(to_np(dv), gv, "dV")
+
+
+def _heads_subset(w, count, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randperm(w.B * w.H, generator=g)[:count].tolist()
+
+
+@pytest.mark.parametrize("w,q_rows,k_rows,k_heads", [
+    (W.CAUSAL_OUTLIERS, 48, 32, 3),
+    (W.LONG_CAUSAL, 256, 32, 1),
+])
+def test_bwd_full_size_sampled(w, q_rows, k_rows, k_heads):
+    """Full-size launch.  dQ is checked on seeded query rows of every head;
+    dK, dV on seeded key rows of a few seeded heads (each needs the whole
+    softmax of every query row of that head).  The per-tensor scale is the
+    max |grad| over the checked rows."""
+    inp = W.make_inputs(w)
+    dq, dk, dv = run_fwd_bwd(inp, w.causal, w.scale)
+    r = W.sample_rows(w, q_rows, seed=w.seed + 2)
+    gq = oracle.attention_backward_query_rows(inp["q"], inp["k"], inp["v"], inp["do"],
+                                              r.numpy(), w.causal, w.scale)
+    check_grad(gather_rows(dq, r), gq, "dQ")
+    heads = _heads_subset(w, k_heads, w.seed + 3)
+    kr = W.sample_rows(w, k_rows, seed=w.seed + 4)
+    for hflat in heads:
+        b, h = divmod(hflat, w.H)
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        sub = {n: inp[n][sl] for n in ("q", "k", "v", "do")}
+        rows = kr[b, h].numpy()
+        gk, gv = oracle.attention_backward_key_rows(sub["q"], sub["k"], sub["v"], sub["do"],
+                                                    rows, w.causal, w.scale)
+        check_grad(to_np(dk[sl])[0, 0, rows], gk[0, 0], f"dK head {hflat}")
+        check_grad(to_np(dv[sl])[0, 0, rows], gv[0, 0], f"dV head {hflat}")
+    # properties that hold at any size (P rows sum to one):
+    # sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i, per head
+    dk64, dv64 = to_np(dk), to_np(dv)
+    do64 = to_np(inp["do"])
+    tol_k = 2.0 ** -7 * np.abs(dk64).sum(axis=2)
+    tol_v = 2.0 ** -7 * np.abs(dv64).sum(axis=2) + 1e-6
+    assert (np.abs(dk64.sum(axis=2)) <= tol_k).all()
+    assert (np.abs(dv64.sum(axis=2) - do64.sum(axis=2)) <= tol_v).all()
+
+
+def test_bwd_preprocess_entry_point():
+    """fattn_bwd_preprocess: D = rowsum(dO o O) in fp32 and a zeroed dQ
+    accumulator (random inputs, checked against an fp64 row sum)."""
+    g = torch.Generator().manual_seed(5)
+    o = torch.randn(2, 3, 77, 128, generator=g).to(torch.bfloat16)
+    do = torch.randn(2, 3, 77, 128, generator=g).to(torch.bfloat16)
+    D = torch.full((2, 3, 77), float("nan"), device="cuda")
+    acc = torch.full((2, 3, 77, 128), float("nan"), device="cuda")
+    A.fattn_bwd_preprocess(o.cuda(), do.cuda(), D, acc)
+    assert A.fattn_check_status() == 0
+    want = (to_np(o) * to_np(do)).sum(-1)
+    assert np.abs(to_np(D) - want).max() <= 1e-4 * max(1.0, np.abs(want).max())
+    assert bool((acc == 0).all())
+
+
+def test_bwd_workspace_reuse_and_stream():
+    """Two backward passes on a side stream with one caller-owned workspace
+    give identical dK, dV (dQ sums atomically, so only its tolerance holds)."""
+    w = W.Workload("ws", 1, 2, 300, 64, True, seed=8)
+    inp = W.make_inputs(w)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        o, lse = A.fattn_fwd(q, k, v, causal=True, scale=w.scale)
+        ws = A.workspace_for(q)
+        r1 = A.fattn_bwd(q, k, v, o, do, lse, causal=True, scale=w.scale, workspace=ws)
+        r1 = [t.clone() for t in r1]
+        r2 = A.fattn_bwd(q, k, v, o, do, lse, causal=True, scale=w.scale, workspace=ws)
+    side.synchronize()
+    assert A.fattn_check_status() == 0
+    assert torch.equal(r1[1], r2[1]) and torch.equal(r1[2], r2[2])
+    gq, _, _, _ = oracle.attention_backward(inp["q"], inp["k"], inp["v"], inp["do"], True, w.scale)
+    check_grad(to_np(r2[0]), gq, "dQ")
