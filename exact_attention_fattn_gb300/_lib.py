@@ -17,6 +17,8 @@ FATTN_ERR_INVALID_ARG = 1
 FATTN_ERR_UNSUPPORTED = 2
 FATTN_ERR_CUDA = 3
 FATTN_ERR_TIMEOUT = 4
+FATTN_ERR_TOO_LARGE = 5
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 _c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
 
@@ -34,6 +36,8 @@ SIGNATURES = {
                                 _c_int, _c_int, _c_int, _c_float, _vp]),
     "fattn_bwd_finish": (_c_int, [_vp, _c_size, _vp, _c_int, _c_int, _c_int, _c_int, _c_float,
                                   _vp]),
+    "fattn_bwd_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int,
+                                   _c_int, _c_int, _c_int, _c_float, _vp]),
     "fattn_check_status": (_c_int, [_vp]),
     "fattn_status_string": (ctypes.c_char_p, [_c_int]),
     "fattn_set_wait_budget": (None, [ctypes.c_longlong]),

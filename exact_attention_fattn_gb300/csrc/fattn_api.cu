@@ -330,6 +330,7 @@ const char* fattn_status_string(int status) {
     case FATTN_ERR_UNSUPPORTED: return "unsupported head dimension or device";
     case FATTN_ERR_CUDA: return "CUDA error";
     case FATTN_ERR_TIMEOUT: return "kernel wait timed out";
+    case FATTN_ERR_TOO_LARGE: return "problem exceeds the built-in scratch of fattn_bwd_noalloc";
     default: return "unknown status";
   }
 }
@@ -357,3 +358,52 @@ int fattn_selftest_timeout(long long budget_cycles, fattn_stream_t stream) {
 const char* fattn_version(void) { return "0.1.0"; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward pass without allocation: its scratch lives in this fixed device
+// array.  In host code the name is only a stand-in for the symbol; the
+// device address comes from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) unsigned char g_fattn_noalloc_scratch[FATTN_NOALLOC_SCRATCH_BYTES];
+
+namespace fattn {
+namespace {
+void* g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+}  // namespace fattn
+
+extern "C" int fattn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                                 const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                                 int B, int H, int N, int d, int causal, float scale,
+                                 fattn_stream_t stream) {
+  int rc = check_sizes(B, H, N, d);
+  if (rc != FATTN_OK) return rc;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FATTN_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return FATTN_ERR_INVALID_ARG;
+  if (bwd_workspace(B, H, N, d).total > FATTN_NOALLOC_SCRATCH_BYTES) return FATTN_ERR_TOO_LARGE;
+  DeviceStatus* status = nullptr;
+  if ((rc = device_setup(&status)) != FATTN_OK) return rc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FATTN_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_fattn_noalloc_scratch) != cudaSuccess || p == nullptr)
+        return FATTN_ERR_CUDA;
+      g_noalloc_ptr[dev] = p;
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // prepare rewrites D, L*log2(e) (padding included) and zeroes the dQ
+  // accumulator, so nothing depends on what the previous call left behind.
+  if ((rc = bwd_prepare_impl(o, dO, lse, scratch, B, H, N, d, st)) != FATTN_OK) return rc;
+  if ((rc = bwd_main_impl(q, k, v, dO, scratch, dk, dv, B, H, N, d, causal, scale, status, st)) !=
+      FATTN_OK)
+    return rc;
+  return bwd_finish_impl(scratch, dq, B, H, N, d, scale, st);
+}

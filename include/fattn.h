@@ -43,7 +43,8 @@ typedef enum {
   FATTN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or scale */
   FATTN_ERR_UNSUPPORTED = 2, /* d not in {64,128}, or the device is not sm_103 */
   FATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
-  FATTN_ERR_TIMEOUT = 4      /* a kernel gave up on a pipeline wait */
+  FATTN_ERR_TIMEOUT = 4,     /* a kernel gave up on a pipeline wait */
+  FATTN_ERR_TOO_LARGE = 5    /* the problem needs more scratch than fattn_bwd_noalloc has */
 } fattn_status;
 
 /*
@@ -120,6 +121,42 @@ int fattn_bwd_main(const void* q, const void* k, const void* v, const void* dO,
                    fattn_stream_t stream);
 int fattn_bwd_finish(const void* workspace, size_t workspace_bytes, void* dq,
                      int B, int H, int N, int d, float scale, fattn_stream_t stream);
+
+/* Size of the scratch array built into the library for fattn_bwd_noalloc. */
+#define FATTN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * Backward pass for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it is a service of the
+ * library.  It does what fattn_bwd does, with the same arguments minus the
+ * workspace, but takes its scratch (D, L*log2(e) and the fp32 dQ
+ * accumulator) from a fixed device array compiled into the library
+ * (FATTN_NOALLOC_SCRATCH_BYTES, 64 MiB, held on every device that loads the
+ * library until the process exits).  It is meant for code that has no way
+ * to obtain device memory at the point of the call: a plugin whose host
+ * framework owns every allocation and forbids the plugin to make its own,
+ * a real-time loop in which cudaMalloc's implicit device synchronisation is
+ * not acceptable, or a caller that simply has no spare buffer to pass.
+ * This call itself never calls cudaMalloc, cudaFree or any allocating
+ * routine.
+ *
+ *  - Size limit: fattn_bwd_workspace_bytes(B,H,N,d) must not exceed
+ *    FATTN_NOALLOC_SCRATCH_BYTES (about B*H*N <= 127,000 at d = 128 and
+ *    <= 250,000 at d = 64); larger problems return FATTN_ERR_TOO_LARGE and
+ *    enqueue nothing.
+ *  - The first call on a device looks up the array's device address (no
+ *    allocation); make that first call before any stream capture begins.
+ *  - Every call on a device uses the same array, and the array keeps the
+ *    last call's contents; the call re-initialises everything it reads.
+ *    Calls whose work overlaps on the GPU (other streams, other host
+ *    threads) race on the array: serialise them.
+ * Returns a fattn_status.
+ */
+int fattn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                      const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                      int B, int H, int N, int d, int causal, float scale,
+                      fattn_stream_t stream);
 
 /*
  * Synchronise `stream`, then report the first error since the last call:
