@@ -13,11 +13,16 @@
 // is converted by a separate kernel.  The dQ and dK formulas follow from
 // S = scale Q K^T by the chain rule (the pages stop at dS).
 //
-// Warps: 0-3 compute (TMEM lanes 0..127), 4 TMEM allocation + MMA issue,
-// 5 TMA producer.
-// TMEM (512 columns): A [0,128) holds S^T, then P^T (bf16, [0,64)), then dQ
-// ([0,d)); B [128,256) holds dP^T, then dS^T (bf16, [128,192)); dV at
-// [256,256+d), dK at [256+d,256+2d).
+// Warps: 0-7 compute, as two warpgroups that split the 128 query columns of
+// every key row (P and dS are elementwise, so the halves never exchange
+// anything); 8 TMEM allocation + MMA issue; 9 TMA producer; 10-11 idle.
+// TMEM (512 columns): A [0,128) holds S^T, then P^T; B [128,256) holds dP^T,
+// then dS^T, then dQ ([128,128+d)).  Each warpgroup packs its 64 bf16 values
+// (32 columns) into the first half of the 64 fp32 columns it read itself
+// (query 0-63 -> [0,32), query 64-127 -> [64,96)), never into columns the
+// other warpgroup may still be reading.
+// dV at [256,256+d), dK at [256+d,256+2d).  With dQ in B, the next S^T can be
+// computed into A while the dQ rows are being read out.
 #include "fattn_internal.h"
 #include "fattn_ptx.cuh"
 
@@ -26,9 +31,10 @@ namespace fattn {
 namespace {
 
 constexpr int kTile = 128;     // rows per Q tile and per K/V tile
-constexpr int kThreads = 192;
-constexpr int kMmaWarp = 4;
-constexpr int kLoadWarp = 5;
+constexpr int kThreads = 384;
+constexpr int kComputeThreads = 256;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
 constexpr uint32_t kColA = 0, kColB = 128, kColDV = 256;
 
 template <int HD>
@@ -112,10 +118,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(kBarSFull), 1);
     mbar_init(bar(kBarDpFull), 1);
-    mbar_init(bar(kBarPFull), 128);
-    mbar_init(bar(kBarDsFull), 128);
+    mbar_init(bar(kBarPFull), kComputeThreads);
+    mbar_init(bar(kBarDsFull), kComputeThreads);
     mbar_init(bar(kBarDqFull), 1);
-    mbar_init(bar(kBarDqEmpty), 128);
+    mbar_init(bar(kBarDqEmpty), kComputeThreads);
     mbar_init(bar(kBarDkvFull), 1);
     mbar_init(bar(kBarMmaDone), 1);
     misc[1] = 0u;
@@ -139,49 +145,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = misc[0];
   const WaitCtx wc{args.wait_budget, reinterpret_cast<volatile uint32_t*>(&misc[1]), args.status};
 
-  if (warp < 4) {
+  if (warp < 8) {
     // ================================================================ compute
-    const int r = warp * 32 + lane;          // kv row of the tile = TMEM lane
+    const int half = warp >> 2;              // query columns [64*half, 64*half + 64)
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;            // kv row of the tile = TMEM lane
     const int kv = kv0 + r;
     const bool kv_valid = kv < N;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tA = tmem + lane_off + kColA;
     const uint32_t tB = tmem + lane_off + kColB;
     const float c = args.scale_log2;
     const uint32_t ds_base = sbase + C::kDsOff;
-    const uint32_t stg = ds_base + warp * 8192;  // per-warp staging for dQ rows
+    const uint32_t stg = ds_base + warp * 4096;  // per-warp staging for dQ rows
+    const int col0 = 64 * half;
     bool ok = true;
     for (int it = 0; it < n_it && ok; ++it) {
       const int i = i0 + it;
       const int q0 = i * kTile;
       const int s = it & 1;
       const uint32_t ph = it & 1;
-      const float* l2s = reinterpret_cast<const float*>(smem + C::kLdOff + s * 1024);
+      const float* l2s = reinterpret_cast<const float*>(smem + C::kLdOff + s * 1024) + col0;
       const float* ds_vec = l2s + 128;
-      // ---- P^T = 2^(S^T c - L2) (masked)
+      // ---- P^T = 2^(S^T c - L2) (masked), this half's 64 query columns
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull), ph, wc, kWaitSFull));
       if (!ok) break;
       tc_fence_after();
-      uint32_t p0[32], p1[32], p2[32], p3[32];
-      tmem_ld32(tA + 0, p0);
-      tmem_ld32(tA + 32, p1);
-      tmem_ld32(tA + 64, p2);
-      tmem_ld32(tA + 96, p3);
+      uint32_t p0[32], p1[32];
+      tmem_ld32(tA + col0, p0);
+      tmem_ld32(tA + col0 + 32, p1);
       tmem_ld_wait32(p0);
       reg_fence32(p1);
-      reg_fence32(p2);
-      reg_fence32(p3);
-      uint32_t* pv[4] = {p0, p1, p2, p3};
+      uint32_t* pv[2] = {p0, p1};
       const bool diag = CAUSAL && q0 == kv0;
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
+      for (int g = 0; g < 2; ++g) {
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(l2s + g * 32 + e);
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int col = g * 32 + e + u;
+            const int col = col0 + g * 32 + e + u;
             float p = ex2_approx(fmaf(__uint_as_float(pv[g][e + u]), c, -lv[u]));
             if (!kv_valid || (diag && col < r)) p = 0.f;
             pv[g][e + u] = __float_as_uint(p);
@@ -191,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           pk[e] = pack_bf16x2(__uint_as_float(pv[g][2 * e]), __uint_as_float(pv[g][2 * e + 1]));
-        tmem_st16(tA + 16 * g, pk);
+        tmem_st16(tA + col0 + 16 * g, pk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -200,11 +205,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDpFull), ph, wc, kWaitDpFull));
       if (!ok) break;
       tc_fence_after();
+      uint32_t dp0[32], dp1[32];
+      tmem_ld32(tB + col0, dp0);
+      tmem_ld32(tB + col0 + 32, dp1);
+      tmem_ld_wait32(dp0);
+      reg_fence32(dp1);
+      uint32_t* dpv[2] = {dp0, dp1};
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        uint32_t dp[32];
-        tmem_ld32(tB + 32 * g, dp);
-        tmem_ld_wait32(dp);
+      for (int g = 0; g < 2; ++g) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
@@ -213,17 +221,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           float dsv[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            dsv[u] = __uint_as_float(pv[g][e + u]) * (__uint_as_float(dp[e + u]) - dv4[u]);
+            dsv[u] = __uint_as_float(pv[g][e + u]) * (__uint_as_float(dpv[g][e + u]) - dv4[u]);
           pk[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
           pk[e / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
         }
-        tmem_st16(tB + 16 * g, pk);
-        // dS row r, q columns [32g, 32g+32) = four 16-byte chunks of the
-        // MN-major (q contiguous) operand: two 64-column atoms, 128-byte
+        tmem_st16(tB + col0 + 16 * g, pk);
+        // dS row r, query columns [col0 + 32g, +32) = four 16-byte chunks of
+        // the MN-major (query-contiguous) operand: 64-column atoms, 128-byte
         // swizzle inside each.
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
-          const int c16 = g * 4 + qq;
+          const int c16 = (col0 >> 3) + g * 4 + qq;
           const uint32_t addr = ds_base + (c16 >> 3) * 16384 + r * 128 +
                                 (static_cast<uint32_t>((c16 & 7) ^ (r & 7)) << 4);
           st_shared_v4(addr, pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
@@ -233,16 +241,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(kBarDsFull));
-      // ---- dQ_i rows (TMEM lane = q row) -> fp32 atomics, through a
-      // per-warp shared-memory transpose so that each atomic instruction
-      // covers four 128-byte row segments.
+      // ---- dQ_i rows (TMEM lane = query row), this half's d/2 columns ->
+      // fp32 atomics, through a per-warp shared-memory transpose so that each
+      // atomic instruction covers four 128-byte row segments.
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDqFull), ph, wc, kWaitDqFull));
       if (!ok) break;
       tc_fence_after();
 #pragma unroll 1
-      for (int ch = 0; ch < HD / 32; ++ch) {
+      for (int ch = half * (HD / 64); ch < (half + 1) * (HD / 64); ++ch) {
         uint32_t dq[32];
-        tmem_ld32(tA + 32 * ch, dq);
+        tmem_ld32(tB + 32 * ch, dq);
         tmem_ld_wait32(dq);
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4)
@@ -254,8 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int rl = k4 * 4 + (lane >> 3);
           const int c4 = lane & 7;
           const float4 v = *reinterpret_cast<const float4*>(
-              smem + C::kDsOff + warp * 8192 + rl * 128 + ((c4 ^ (rl & 7)) << 4));
-          const int q = q0 + warp * 32 + rl;
+              smem + C::kDsOff + warp * 4096 + rl * 128 + ((c4 ^ (rl & 7)) << 4));
+          const int q = q0 + wq * 32 + rl;
           if (q < N)
             atomicAdd(reinterpret_cast<float4*>(
                           args.dq_accum + (static_cast<size_t>(bh) * N + q) * HD + ch * 32 + c4 * 4),
@@ -266,45 +274,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(kBarDqEmpty));
     }
-    // ---- epilogue: dV_j, dK_j * scale -> bf16 -> K/V shared memory -> TMA
+    // ---- epilogue: warpgroup 0 stores dV_j, warpgroup 1 stores dK_j * scale
+    // (bf16, staged in the V / K tiles' shared memory, then TMA)
     if (ok) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDkvFull), 0, wc, kWaitOFull));
       if (ok) {
         tc_fence_after();
+        const uint32_t tsrc = tmem + lane_off + (half == 0 ? kColDV : C::kColDK);
+        const float mul = half == 0 ? 1.f : args.scale;
+        const uint32_t stage = sbase + (half == 0 ? C::kVOff : C::kKOff);
 #pragma unroll 1
-        for (int which = 0; which < 2; ++which) {
-          const uint32_t tsrc = tmem + lane_off + (which == 0 ? kColDV : C::kColDK);
-          const float mul = which == 0 ? 1.f : args.scale;
-          const uint32_t stage = sbase + (which == 0 ? C::kVOff : C::kKOff);
-#pragma unroll 1
-          for (int ch = 0; ch < HD / 32; ++ch) {
-            uint32_t o[32];
-            tmem_ld32(tsrc + 32 * ch, o);
-            tmem_ld_wait32(o);
-            uint32_t pk[16];
+        for (int ch = 0; ch < HD / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(tsrc + 32 * ch, o);
+          tmem_ld_wait32(o);
+          uint32_t pk[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * mul,
-                                  __uint_as_float(o[2 * e + 1]) * mul);
-            const uint32_t rowaddr = stage + (ch >> 1) * C::kChunkBytes + r * 128;
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * mul,
+                                __uint_as_float(o[2 * e + 1]) * mul);
+          const uint32_t rowaddr = stage + (ch >> 1) * C::kChunkBytes + r * 128;
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-              const uint32_t chunk = (ch & 1) * 4 + qq;
-              st_shared_v4(rowaddr + ((chunk ^ (r & 7)) << 4), pk[4 * qq], pk[4 * qq + 1],
-                           pk[4 * qq + 2], pk[4 * qq + 3]);
-            }
+          for (int qq = 0; qq < 4; ++qq) {
+            const uint32_t chunk = (ch & 1) * 4 + qq;
+            st_shared_v4(rowaddr + ((chunk ^ (r & 7)) << 4), pk[4 * qq], pk[4 * qq + 1],
+                         pk[4 * qq + 2], pk[4 * qq + 3]);
           }
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0 && kv0 + warp * 32 < N) {
+        if (lane == 0 && kv0 + wq * 32 < N) {
+          const CUtensorMap* tm = half == 0 ? &tm_dv : &tm_dk;
 #pragma unroll
-          for (int cc = 0; cc < C::kChunks; ++cc) {
-            tma_store_3d(&tm_dv, sbase + C::kVOff + cc * C::kChunkBytes + warp * 32 * 128,
-                         cc * 64, kv0 + warp * 32, bh);
-            tma_store_3d(&tm_dk, sbase + C::kKOff + cc * C::kChunkBytes + warp * 32 * 128,
-                         cc * 64, kv0 + warp * 32, bh);
-          }
+          for (int cc = 0; cc < C::kChunks; ++cc)
+            tma_store_3d(tm, stage + cc * C::kChunkBytes + wq * 32 * 128, cc * 64, kv0 + wq * 32,
+                         bh);
           bulk_commit_group();
           bulk_wait_group_read0();
         }
@@ -330,11 +334,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       // D(128 x HD) (+)= A(tmem, 128 x 128) B, B MN-major (HD contiguous).
+      // A's 16-query K steps sit at columns 8*kk for queries 0-63 and at
+      // 64 + 8*(kk-4) for queries 64-127 (see the TMEM layout above).
       auto mma_tmem_a = [&](uint32_t d, uint32_t a_col, uint32_t b, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(d, tmem + a_col + 8 * kk, sdesc_sw128(b + kk * 2048, C::kChunkBytes, 1024),
-                 idesc_tm, (acc || kk > 0) ? 1u : 0u);
+          mma_ts(d, tmem + a_col + (kk >> 2) * 64 + (kk & 3) * 8,
+                 sdesc_sw128(b + kk * 2048, C::kChunkBytes, 1024), idesc_tm,
+                 (acc || kk > 0) ? 1u : 0u);
       };
       auto qfull = [&](int it) {
         return mbar_wait(bar(kBarQFull + (it & 1)), (it >> 1) & 1, wc, kWaitKvFull);
@@ -355,10 +362,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar(kBarDsFull), ph, wc, kWaitDsFull)) goto mma_end;
         tc_fence_after();
         mma_tmem_a(tmem + C::kColDK, kColB, sQ(s), it > 0);     // dK += dS^T Q
-        // dQ = dS K: A = dS (q contiguous, MN-major), B = K (HD contiguous).
+        // dQ = dS K into B (dS^T there has just been consumed by the dK MMA,
+        // issued before): A = dS (q contiguous, MN-major), B = K (HD contiguous).
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ss(tmem + kColA, sdesc_sw128(sDs + kk * 2048, 16384, 1024),
+          mma_ss(tmem + kColB, sdesc_sw128(sDs + kk * 2048, 16384, 1024),
                  sdesc_sw128(sK + kk * 2048, C::kChunkBytes, 1024), idesc_mm,
                  kk > 0 ? 1u : 0u);
         mma_commit(bar(kBarDqFull));
@@ -366,12 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it + 1 < n_it) {
           if (!qfull(it + 1)) goto mma_end;
           tc_fence_after();
-          mma_kmajor(tmem + kColB, sV, sDo(s ^ 1));             // dP^T (next)
-          mma_commit(bar(kBarDpFull));
+          mma_kmajor(tmem + kColA, sK, sQ(s ^ 1));              // S^T (next), overlaps the dQ read-out
+          mma_commit(bar(kBarSFull));
           if (!mbar_wait(bar(kBarDqEmpty), ph, wc, kWaitDqEmpty)) goto mma_end;
           tc_fence_after();
-          mma_kmajor(tmem + kColA, sK, sQ(s ^ 1));              // S^T (next)
-          mma_commit(bar(kBarSFull));
+          mma_kmajor(tmem + kColB, sV, sDo(s ^ 1));             // dP^T (next)
+          mma_commit(bar(kBarDpFull));
         }
       }
       mma_commit(bar(kBarDkvFull));

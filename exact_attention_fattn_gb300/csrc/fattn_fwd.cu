@@ -34,6 +34,14 @@ constexpr int kThreads = 384;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr float kLn2 = 0.69314718055994530942f;
+// Register split: the kernel launches with kLaunchRegs per thread (384 x 168 =
+// 64,512); the control warpgroup (warps 8-11) gives back down to kCtrlRegs and
+// the two softmax warpgroups grow to kSoftmaxRegs: 128 x 56 + 256 x 224 =
+// 64,512, exactly the launch total, so setmaxnreg.inc can always complete.
+constexpr int kLaunchRegs = 168;
+constexpr int kCtrlRegs = 56;
+constexpr int kSoftmaxRegs = 224;
+static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs == kThreads * kLaunchRegs, "register split");
 
 template <int HD>
 struct FwdCfg {
@@ -135,6 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtx wc{args.wait_budget, reinterpret_cast<volatile uint32_t*>(&misc[1]), args.status};
 
   if (warp < 8) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     // ================================================================ softmax
     const int t = warp >> 2;
     const int wq = warp & 3;
@@ -178,12 +187,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      float mx = -INFINITY;
+      // Row max as four independent 3-input max chains (one per 32-column
+      // group), so the reduction is not one 128-long dependent chain.
+      float mg[4];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
+        float a = fmax3(__uint_as_float(sv[g][0]), __uint_as_float(sv[g][1]),
+                        __uint_as_float(sv[g][2]));
+        float b2 = fmax3(__uint_as_float(sv[g][3]), __uint_as_float(sv[g][4]),
+                         __uint_as_float(sv[g][5]));
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sv[g][i]));
+        for (int i = 6; i < 30; i += 4) {
+          a = fmax3(a, __uint_as_float(sv[g][i]), __uint_as_float(sv[g][i + 1]));
+          b2 = fmax3(b2, __uint_as_float(sv[g][i + 2]), __uint_as_float(sv[g][i + 3]));
+        }
+        mg[g] = fmax3(a, b2, fmaxf(__uint_as_float(sv[g][30]), __uint_as_float(sv[g][31])));
       }
+      const float mx = fmaxf(fmax3(mg[0], mg[1], mg[2]), mg[3]);
       const float m_new = mx * c;
       const bool need = m_new > m_ref + tau;
       if (__any_sync(0xffffffffu, need)) {
@@ -207,26 +227,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float neg_m = -m_ref;
-      float rs = 0.f, rs_bf = 0.f;
+      // Partial sums per 32-column group keep the additions independent.
+      float rs[4], rs_bf[4];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         uint32_t pk[16];
+        float e0 = 0.f, e1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float a0 = ex2_approx(fmaf(__uint_as_float(sv[g][2 * i]), c, neg_m));
           const float a1 = ex2_approx(fmaf(__uint_as_float(sv[g][2 * i + 1]), c, neg_m));
           pk[i] = pack_bf16x2(a0, a1);
-          rs += a0 + a1;
+          e0 += a0;
+          e1 += a1;
           // O is divided by the sum of the bf16 values that P V actually
           // used, so that O is a convex combination of V rows with the
           // rounded weights (exact for a row dominated by one key); L keeps
           // the fp32 sum.
-          rs_bf += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
+          b0 += __uint_as_float(pk[i] << 16);
+          b1 += __uint_as_float(pk[i] & 0xffff0000u);
         }
         tmem_st16(tP + 16 * g, pk);
+        rs[g] = e0 + e1;
+        rs_bf[g] = b0 + b1;
       }
-      l += rs;
-      l_bf += rs_bf;
+      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      l_bf += (rs_bf[0] + rs_bf[1]) + (rs_bf[2] + rs_bf[3]);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(b.p_full[t]);
@@ -271,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kMmaWarp) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
     // ================================================================ MMA issue
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false, false);
@@ -353,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == kLoadWarp) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
     // ================================================================ TMA producer
     if (lane == 0) {
       int issued = 0;
@@ -384,6 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(b.q_full, 0, args.wait_budget);
     }
     __syncwarp();
+  } else {
+    // warps 10-11: no work; they only hand their registers back.
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
   }
 
   tc_fence_before();
@@ -402,6 +433,11 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
+  // The register split inside the kernel is only valid for this launch size.
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   const int num_pairs = (a.N + 2 * kBM - 1) / (2 * kBM);
   const dim3 grid(static_cast<unsigned>(num_pairs * a.BH));
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, a);
