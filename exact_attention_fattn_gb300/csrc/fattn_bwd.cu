@@ -72,15 +72,6 @@ enum : int {
   kBarMmaDone = 12,
 };
 
-__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
-                                             uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 template <int HD, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -317,7 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ================================================================ MMA issue
-    if (lane == 0) {
+    // The whole warp runs this (converged); one elected lane issues.
+    {
       constexpr uint32_t idesc_kk = idesc_bf16_f32(kTile, kTile, false, false);
       constexpr uint32_t idesc_tm = idesc_bf16_f32(kTile, HD, false, true);
       constexpr uint32_t idesc_mm = idesc_bf16_f32(kTile, HD, true, true);
@@ -326,92 +318,100 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto sDo = [&](int s) { return sbase + C::kStageOff + s * C::kStageBytes + C::kTileBytes; };
       // D(128 x 128) = A(128 x HD) B(128 x HD)^T, both K-major (HD contiguous).
       auto mma_kmajor = [&](uint32_t d, uint32_t a, uint32_t b) {
+        const uint64_t da = sdesc_sw128(a, 16, 1024), db = sdesc_sw128(b, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          mma_ss(d, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), idesc_kk,
-                 kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+          mma_ss_w(d, da + off, db + off, idesc_kk, kk > 0 ? 1u : 0u);
         }
       };
       // D(128 x HD) (+)= A(tmem, 128 x 128) B, B MN-major (HD contiguous).
       // A's 16-query K steps sit at columns 8*kk for queries 0-63 and at
       // 64 + 8*(kk-4) for queries 64-127 (see the TMEM layout above).
-      auto mma_tmem_a = [&](uint32_t d, uint32_t a_col, uint32_t b, bool acc) {
+      auto mma_tmem_a = [&](uint32_t d, uint32_t a_col, uint32_t b, uint32_t acc) {
+        const uint64_t db = sdesc_sw128(b, C::kChunkBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(d, tmem + a_col + (kk >> 2) * 64 + (kk & 3) * 8,
-                 sdesc_sw128(b + kk * 2048, C::kChunkBytes, 1024), idesc_tm,
-                 (acc || kk > 0) ? 1u : 0u);
+          mma_ts_w(d, tmem + a_col + (kk >> 2) * 64 + (kk & 3) * 8, db + ((kk * 2048) >> 4),
+                   idesc_tm, kk > 0 ? 1u : acc);
       };
       auto qfull = [&](int it) {
-        return mbar_wait(bar(kBarQFull + (it & 1)), (it >> 1) & 1, wc, kWaitKvFull);
+        return mbar_wait_warp(bar(kBarQFull + (it & 1)), (it >> 1) & 1, wc, kWaitKvFull);
       };
-      if (!mbar_wait(bar(kBarKv), 0, wc, kWaitKvFull)) goto mma_end;
+      if (!mbar_wait_warp(bar(kBarKv), 0, wc, kWaitKvFull)) goto mma_end;
       if (!qfull(0)) goto mma_end;
       tc_fence_after();
       mma_kmajor(tmem + kColA, sK, sQ(0));   // S^T
-      mma_commit(bar(kBarSFull));
+      mma_commit_w(bar(kBarSFull));
       mma_kmajor(tmem + kColB, sV, sDo(0));  // dP^T
-      mma_commit(bar(kBarDpFull));
+      mma_commit_w(bar(kBarDpFull));
       for (int it = 0; it < n_it; ++it) {
         const int s = it & 1;
         const uint32_t ph = it & 1;
-        if (!mbar_wait(bar(kBarPFull), ph, wc, kWaitPFull)) goto mma_end;
+        const uint32_t acc = it > 0 ? 1u : 0u;
+        if (!mbar_wait_warp(bar(kBarPFull), ph, wc, kWaitPFull)) goto mma_end;
         tc_fence_after();
-        mma_tmem_a(tmem + kColDV, kColA, sDo(s), it > 0);       // dV += P^T dO
-        if (!mbar_wait(bar(kBarDsFull), ph, wc, kWaitDsFull)) goto mma_end;
+        mma_tmem_a(tmem + kColDV, kColA, sDo(s), acc);           // dV += P^T dO
+        if (!mbar_wait_warp(bar(kBarDsFull), ph, wc, kWaitDsFull)) goto mma_end;
         tc_fence_after();
-        mma_tmem_a(tmem + C::kColDK, kColB, sQ(s), it > 0);     // dK += dS^T Q
+        mma_tmem_a(tmem + C::kColDK, kColB, sQ(s), acc);         // dK += dS^T Q
         // dQ = dS K into B (dS^T there has just been consumed by the dK MMA,
         // issued before): A = dS (q contiguous, MN-major), B = K (HD contiguous).
+        {
+          const uint64_t da = sdesc_sw128(sDs, 16384, 1024);
+          const uint64_t db = sdesc_sw128(sK, C::kChunkBytes, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ss(tmem + kColB, sdesc_sw128(sDs + kk * 2048, 16384, 1024),
-                 sdesc_sw128(sK + kk * 2048, C::kChunkBytes, 1024), idesc_mm,
-                 kk > 0 ? 1u : 0u);
-        mma_commit(bar(kBarDqFull));
-        mma_commit(bar(kBarQEmpty + s));
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ss_w(tmem + kColB, da + ((kk * 2048) >> 4), db + ((kk * 2048) >> 4), idesc_mm,
+                     kk > 0 ? 1u : 0u);
+        }
+        mma_commit_w(bar(kBarDqFull));
+        mma_commit_w(bar(kBarQEmpty + s));
         if (it + 1 < n_it) {
           if (!qfull(it + 1)) goto mma_end;
           tc_fence_after();
-          mma_kmajor(tmem + kColA, sK, sQ(s ^ 1));              // S^T (next), overlaps the dQ read-out
-          mma_commit(bar(kBarSFull));
-          if (!mbar_wait(bar(kBarDqEmpty), ph, wc, kWaitDqEmpty)) goto mma_end;
+          mma_kmajor(tmem + kColA, sK, sQ(s ^ 1));               // S^T (next), overlaps the dQ read-out
+          mma_commit_w(bar(kBarSFull));
+          if (!mbar_wait_warp(bar(kBarDqEmpty), ph, wc, kWaitDqEmpty)) goto mma_end;
           tc_fence_after();
-          mma_kmajor(tmem + kColB, sV, sDo(s ^ 1));             // dP^T (next)
-          mma_commit(bar(kBarDpFull));
+          mma_kmajor(tmem + kColB, sV, sDo(s ^ 1));              // dP^T (next)
+          mma_commit_w(bar(kBarDpFull));
         }
       }
-      mma_commit(bar(kBarDkvFull));
+      mma_commit_w(bar(kBarDkvFull));
     mma_end:
-      mma_commit(bar(kBarMmaDone));
+      mma_commit_w(bar(kBarMmaDone));
       mbar_wait_drain(bar(kBarMmaDone), 0, args.wait_budget);
     }
     __syncwarp();
   } else if (warp == kLoadWarp) {
     // ================================================================ TMA producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar(kBarKv), 2 * C::kTileBytes);
+    // Converged warp; one elected lane issues each copy.
+    {
+      mbar_arrive_expect_tx_w(bar(kBarKv), 2 * C::kTileBytes);
       for (int cc = 0; cc < C::kChunks; ++cc) {
-        tma_load_3d(sbase + C::kKOff + cc * C::kChunkBytes, &tm_k, bar(kBarKv), cc * 64, kv0, bh);
-        tma_load_3d(sbase + C::kVOff + cc * C::kChunkBytes, &tm_v, bar(kBarKv), cc * 64, kv0, bh);
+        tma_load_3d_w(sbase + C::kKOff + cc * C::kChunkBytes, &tm_k, bar(kBarKv), cc * 64, kv0,
+                      bh);
+        tma_load_3d_w(sbase + C::kVOff + cc * C::kChunkBytes, &tm_v, bar(kBarKv), cc * 64, kv0,
+                      bh);
       }
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
         const int s = it & 1;
         const int rnd = it >> 1;
-        if (rnd > 0 && !mbar_wait(bar(kBarQEmpty + s), (rnd - 1) & 1, wc, kWaitKvEmpty)) break;
+        if (rnd > 0 && !mbar_wait_warp(bar(kBarQEmpty + s), (rnd - 1) & 1, wc, kWaitKvEmpty))
+          break;
         const uint32_t full = bar(kBarQFull + s);
-        mbar_arrive_expect_tx(full, 2 * C::kTileBytes + 1024);
+        mbar_arrive_expect_tx_w(full, 2 * C::kTileBytes + 1024);
         const int q0 = (i0 + it) * kTile;
         const uint32_t dst = sbase + C::kStageOff + s * C::kStageBytes;
         for (int cc = 0; cc < C::kChunks; ++cc) {
-          tma_load_3d(dst + cc * C::kChunkBytes, &tm_q, full, cc * 64, q0, bh);
-          tma_load_3d(dst + C::kTileBytes + cc * C::kChunkBytes, &tm_do, full, cc * 64, q0, bh);
+          tma_load_3d_w(dst + cc * C::kChunkBytes, &tm_q, full, cc * 64, q0, bh);
+          tma_load_3d_w(dst + C::kTileBytes + cc * C::kChunkBytes, &tm_do, full, cc * 64, q0, bh);
         }
         const size_t vec = static_cast<size_t>(bh) * pitch + q0;
-        bulk_load_1d(sbase + C::kLdOff + s * 1024, args.L2 + vec, 512, full);
-        bulk_load_1d(sbase + C::kLdOff + s * 1024 + 512, args.D + vec, 512, full);
+        bulk_load_1d_w(sbase + C::kLdOff + s * 1024, args.L2 + vec, 512, full);
+        bulk_load_1d_w(sbase + C::kLdOff + s * 1024 + 512, args.D + vec, 512, full);
         issued = it + 1;
       }
       for (int it = max(0, issued - 2); it < issued; ++it)

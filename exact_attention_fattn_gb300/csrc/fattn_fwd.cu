@@ -36,11 +36,11 @@ constexpr int kLoadWarp = 9;
 constexpr float kLn2 = 0.69314718055994530942f;
 // Register split: the kernel launches with kLaunchRegs per thread (384 x 168 =
 // 64,512); the control warpgroup (warps 8-11) gives back down to kCtrlRegs and
-// the two softmax warpgroups grow to kSoftmaxRegs: 128 x 56 + 256 x 224 =
+// the two softmax warpgroups grow to kSoftmaxRegs: 128 x 72 + 256 x 216 =
 // 64,512, exactly the launch total, so setmaxnreg.inc can always complete.
 constexpr int kLaunchRegs = 168;
-constexpr int kCtrlRegs = 56;
-constexpr int kSoftmaxRegs = 224;
+constexpr int kCtrlRegs = 72;
+constexpr int kSoftmaxRegs = 216;
 static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs == kThreads * kLaunchRegs, "register split");
 
 template <int HD>
@@ -299,7 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
     // ================================================================ MMA issue
-    if (lane == 0) {
+    // The whole warp runs this (converged); one elected lane issues.
+    {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, HD, false, true);
       auto kv_smem = [&](int i) {
@@ -309,103 +310,103 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto kv_empty = [&](int i) { return b.kv_empty0 + 8u * (i % C::kStages); };
       auto kv_parity = [&](int i) { return static_cast<uint32_t>((i / C::kStages) & 1); };
       // S_t = Q_t K^T: M = 128, N = 128, K = HD in steps of 16 (32 bytes
-      // inside a 128-byte swizzle row, then the next 64-column chunk).
+      // inside a 128-byte swizzle row, then the next 64-column chunk).  The
+      // descriptors are built once and advanced by constant offsets (their
+      // start-address field is in 16-byte units).
       auto issue_s = [&](int t, int ik) {
-        const uint32_t qa = sbase + C::kQOff + t * C::kTileBytes;
-        const uint32_t kb = kv_smem(ik);
+        const uint64_t da = sdesc_sw128(sbase + C::kQOff + t * C::kTileBytes, 16, 1024);
+        const uint64_t db = sdesc_sw128(kv_smem(ik), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::col_s(t), sdesc_sw128(qa + off, 16, 1024),
-                 sdesc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+          mma_ss_w(tmem + C::col_s(t), da + off, db + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
       // O_t += P_t V: A = P_t from TMEM (8 columns per K step of 16), B = V
       // tile, MN-major (d contiguous): K step = 16 rows = 2048 bytes, the
       // next 64 columns of d are one chunk (16 KiB) away.
-      auto issue_pv = [&](int t, int iv, bool acc) {
-        const uint32_t vb = kv_smem(iv);
+      auto issue_pv = [&](int t, int iv, uint32_t acc) {
+        const uint64_t dv = sdesc_sw128(kv_smem(iv), C::kChunkBytes, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          mma_ts(tmem + C::col_o(t), tmem + C::col_p(t) + 8 * kk,
-                 sdesc_sw128(vb + kk * 2048, C::kChunkBytes, 1024), idesc_pv,
-                 (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts_w(tmem + C::col_o(t), tmem + C::col_p(t) + 8 * kk, dv + ((kk * 2048) >> 4),
+                   idesc_pv, kk > 0 ? 1u : acc);
       };
-      if (!mbar_wait(b.q_full, 0, wc, kWaitQFull)) goto mma_end;
-      if (!mbar_wait(kv_full(0), kv_parity(0), wc, kWaitKvFull)) goto mma_end;
+      if (!mbar_wait_warp(b.q_full, 0, wc, kWaitQFull)) goto mma_end;
+      if (!mbar_wait_warp(kv_full(0), kv_parity(0), wc, kWaitKvFull)) goto mma_end;
       tc_fence_after();
       for (int t = 0; t < 2; ++t) {
         if (n_t[t] > 0) {
           issue_s(t, 0);
-          mma_commit(b.s_full[t]);
+          mma_commit_w(b.s_full[t]);
         }
       }
-      mma_commit(kv_empty(0));
+      mma_commit_w(kv_empty(0));
       for (int j = 0; j < nt; ++j) {
         const int iv = 2 * j + 1;
         const int ikn = 2 * j + 2;
-        if (!mbar_wait(kv_full(iv), kv_parity(iv), wc, kWaitKvFull)) goto mma_end;
+        if (!mbar_wait_warp(kv_full(iv), kv_parity(iv), wc, kWaitKvFull)) goto mma_end;
         if (j < n_t[0]) {
-          if (!mbar_wait(b.p_full[0], j & 1, wc, kWaitPFull)) goto mma_end;
+          if (!mbar_wait_warp(b.p_full[0], j & 1, wc, kWaitPFull)) goto mma_end;
           tc_fence_after();
-          issue_pv(0, iv, j > 0);
-          if (j == n_t[0] - 1) mma_commit(b.o_full[0]);
+          issue_pv(0, iv, j > 0 ? 1u : 0u);
+          if (j == n_t[0] - 1) mma_commit_w(b.o_full[0]);
         }
         if (j + 1 < nt) {
-          if (!mbar_wait(kv_full(ikn), kv_parity(ikn), wc, kWaitKvFull)) goto mma_end;
+          if (!mbar_wait_warp(kv_full(ikn), kv_parity(ikn), wc, kWaitKvFull)) goto mma_end;
           tc_fence_after();
         }
         if (j + 1 < n_t[0]) {
           issue_s(0, ikn);
-          mma_commit(b.s_full[0]);
+          mma_commit_w(b.s_full[0]);
         }
         if (j < n_t[1]) {
-          if (!mbar_wait(b.p_full[1], j & 1, wc, kWaitPFull)) goto mma_end;
+          if (!mbar_wait_warp(b.p_full[1], j & 1, wc, kWaitPFull)) goto mma_end;
           tc_fence_after();
-          issue_pv(1, iv, j > 0);
-          if (j == n_t[1] - 1) mma_commit(b.o_full[1]);
+          issue_pv(1, iv, j > 0 ? 1u : 0u);
+          if (j == n_t[1] - 1) mma_commit_w(b.o_full[1]);
         }
-        mma_commit(kv_empty(iv));
+        mma_commit_w(kv_empty(iv));
         if (j + 1 < n_t[1]) {
           issue_s(1, ikn);
-          mma_commit(b.s_full[1]);
+          mma_commit_w(b.s_full[1]);
         }
-        if (j + 1 < nt) mma_commit(kv_empty(ikn));
+        if (j + 1 < nt) mma_commit_w(kv_empty(ikn));
       }
     mma_end:
       // No MMA may still be running when TMEM is released.
-      mma_commit(b.mma_done);
+      mma_commit_w(b.mma_done);
       mbar_wait_drain(b.mma_done, 0, args.wait_budget);
     }
     __syncwarp();
   } else if (warp == kLoadWarp) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
     // ================================================================ TMA producer
-    if (lane == 0) {
+    // Converged warp; one elected lane issues each copy.
+    {
       int issued = 0;
       uint32_t qbytes = 0;
       for (int t = 0; t < 2; ++t) qbytes += n_t[t] > 0 ? C::kTileBytes : 0;
-      mbar_arrive_expect_tx(b.q_full, qbytes);
+      mbar_arrive_expect_tx_w(b.q_full, qbytes);
       for (int t = 0; t < 2; ++t) {
         if (n_t[t] == 0) continue;
         for (int cc = 0; cc < C::kChunks; ++cc)
-          tma_load_3d(sbase + C::kQOff + t * C::kTileBytes + cc * C::kChunkBytes, &tm_q, b.q_full,
-                      cc * 64, q0 + t * kBM, bh);
+          tma_load_3d_w(sbase + C::kQOff + t * C::kTileBytes + cc * C::kChunkBytes, &tm_q,
+                        b.q_full, cc * 64, q0 + t * kBM, bh);
       }
       for (int i = 0; i < 2 * nt; ++i) {
         const int s = i % C::kStages;
         const int r = i / C::kStages;
-        if (r > 0 && !mbar_wait(b.kv_empty0 + 8u * s, (r - 1) & 1, wc, kWaitKvEmpty)) break;
+        if (r > 0 && !mbar_wait_warp(b.kv_empty0 + 8u * s, (r - 1) & 1, wc, kWaitKvEmpty)) break;
         const uint32_t full = b.kv_full0 + 8u * s;
-        mbar_arrive_expect_tx(full, C::kTileBytes);
+        mbar_arrive_expect_tx_w(full, C::kTileBytes);
         const CUtensorMap* tm = (i & 1) ? &tm_v : &tm_k;
         const uint32_t dst = sbase + C::kKvOff + s * C::kTileBytes;
         for (int cc = 0; cc < C::kChunks; ++cc)
-          tma_load_3d(dst + cc * C::kChunkBytes, tm, full, cc * 64, (i >> 1) * kBN, bh);
+          tma_load_3d_w(dst + cc * C::kChunkBytes, tm, full, cc * 64, (i >> 1) * kBN, bh);
         issued = i + 1;
       }
-      // Every copy this thread started must have landed before the CTA exits.
+      // Every copy this warp started must have landed before the CTA exits.
       for (int i = max(0, issued - C::kStages); i < issued; ++i)
         mbar_wait_drain(b.kv_full0 + 8u * (i % C::kStages), (i / C::kStages) & 1,
                         args.wait_budget);
