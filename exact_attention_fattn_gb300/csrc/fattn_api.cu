@@ -134,7 +134,7 @@ int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, 
                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
-// Workspace of the backward pass: D and L*log2(e) in a [B*H, Np] layout
+// Workspace of the backward pass: D and -L*log2(e) in a [B*H, Np] layout
 // (Np = N rounded up to the 128-row tile, so that every tile's 512-byte
 // slice can be fetched by one bulk copy), then the fp32 dQ accumulator.
 }  // extern "C"
@@ -399,7 +399,7 @@ extern "C" int fattn_bwd_noalloc(const void* q, const void* k, const void* v, co
     scratch = g_noalloc_ptr[dev];
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // prepare rewrites D, L*log2(e) (padding included) and zeroes the dQ
+  // prepare rewrites D, -L*log2(e) (padding included) and zeroes the dQ
   // accumulator, so nothing depends on what the previous call left behind.
   if ((rc = bwd_prepare_impl(o, dO, lse, scratch, B, H, N, d, st)) != FATTN_OK) return rc;
   if ((rc = bwd_main_impl(q, k, v, dO, scratch, dk, dv, B, H, N, d, causal, scale, status, st)) !=

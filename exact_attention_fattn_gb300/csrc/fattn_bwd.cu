@@ -4,7 +4,7 @@
 // a 128-row K/V tile j of one (batch, head) and walks the 128-row Q tiles i
 // (i >= j when causal).  Per step, with the kv rows on TMEM lanes:
 //   S^T  = K_j Q_i^T                    (tcgen05, fp32 in TMEM)
-//   P^T  = 2^(S^T*scale*log2e - L_i*log2e)    (one thread per kv row; bf16 back to TMEM)
+//   P^T  = 2^(S^T*scale*log2e - L_i*log2e)    (one thread per kv row and query half; bf16 back to TMEM)
 //   dP^T = V_j dO_i^T                   (tcgen05)
 //   dS^T = P^T o (dP^T - D_i)           (bf16 to TMEM and, as dS, to shared memory)
 //   dV_j += P^T dO_i,  dK_j += dS^T Q_i (tcgen05, accumulators in TMEM)
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tA = tmem + lane_off + kColA;
     const uint32_t tB = tmem + lane_off + kColB;
-    const float c = args.scale_log2;
+    const uint64_t c2 = splat2(args.scale_log2);
     const uint32_t ds_base = sbase + C::kDsOff;
     const uint32_t stg = ds_base + warp * 4096;  // per-warp staging for dQ rows
     const int col0 = 64 * half;
@@ -156,8 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q0 = i * kTile;
       const int s = it & 1;
       const uint32_t ph = it & 1;
-      const float* l2s = reinterpret_cast<const float*>(smem + C::kLdOff + s * 1024) + col0;
-      const float* ds_vec = l2s + 128;
+      const uint32_t* nl2s =
+          reinterpret_cast<const uint32_t*>(smem + C::kLdOff + s * 1024) + col0;
+      const uint32_t* ds_vec = nl2s + 128;
       // ---- P^T = 2^(S^T c - L2) (masked), this half's 64 query columns
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull), ph, wc, kWaitSFull));
       if (!ok) break;
@@ -173,12 +174,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int g = 0; g < 2; ++g) {
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(l2s + g * 32 + e);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          // nl2 = -L*log2(e) per query column (-inf past N)
+          const uint4 l4 = *reinterpret_cast<const uint4*>(nl2s + g * 32 + e);
+          uint32_t x[4];
+          unpack2(ffma2(pack2(pv[g][e], pv[g][e + 1]), c2, pack2(l4.x, l4.y)), x[0], x[1]);
+          unpack2(ffma2(pack2(pv[g][e + 2], pv[g][e + 3]), c2, pack2(l4.z, l4.w)), x[2], x[3]);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int col = col0 + g * 32 + e + u;
-            float p = ex2_approx(fmaf(__uint_as_float(pv[g][e + u]), c, -lv[u]));
+            float p = ex2_approx(__uint_as_float(x[u]));
             if (!kv_valid || (diag && col < r)) p = 0.f;
             pv[g][e + u] = __float_as_uint(p);
           }
@@ -207,14 +211,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(ds_vec + g * 32 + e);
-          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-          float dsv[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            dsv[u] = __uint_as_float(pv[g][e + u]) * (__uint_as_float(dpv[g][e + u]) - dv4[u]);
-          pk[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
-          pk[e / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+          const uint4 d4 = *reinterpret_cast<const uint4*>(ds_vec + g * 32 + e);
+          uint32_t y[4];
+          unpack2(fmul2(pack2(pv[g][e], pv[g][e + 1]),
+                        fsub2(pack2(dpv[g][e], dpv[g][e + 1]), pack2(d4.x, d4.y))),
+                  y[0], y[1]);
+          unpack2(fmul2(pack2(pv[g][e + 2], pv[g][e + 3]),
+                        fsub2(pack2(dpv[g][e + 2], dpv[g][e + 3]), pack2(d4.z, d4.w))),
+                  y[2], y[3]);
+          pk[e / 2] = pack_bf16x2(__uint_as_float(y[0]), __uint_as_float(y[1]));
+          pk[e / 2 + 1] = pack_bf16x2(__uint_as_float(y[2]), __uint_as_float(y[3]));
         }
         tmem_st16(tB + col0 + 16 * g, pk);
         // dS row r, query columns [col0 + 32g, +32) = four 16-byte chunks of

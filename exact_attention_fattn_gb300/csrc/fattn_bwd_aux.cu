@@ -32,9 +32,9 @@ __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b) {
 // and zeroes 32 bytes of the accumulator row.  Rows are walked in a padded
 // index space of `pitch` rows per head: row n < N of head bh gets
 //   D[bh*pitch + n]  = sum_k dO O,
-//   L2[bh*pitch + n] = lse[bh*N + n] * log2(e)      (when L2 is given),
-// and the padding rows n >= N get D = 0 and L2 = +inf (a column that no
-// probability can reach: 2^(s - inf) = 0).
+//   L2[bh*pitch + n] = -lse[bh*N + n] * log2(e)      (when L2 is given),
+// and the padding rows n >= N get D = 0 and L2 = -inf (a column that no
+// probability can reach: 2^(s*scale*log2e - inf) = 0).
 template <int HD>
 __global__ void __launch_bounds__(kAuxThreads) preprocess_kernel(
     const uint4* __restrict__ o, const uint4* __restrict__ dO, const float* __restrict__ lse,
@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kAuxThreads) preprocess_kernel(
     for (int off = kTpr / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (in_range && sub == 0) {
       D[prow] = s;
-      if (L2 != nullptr) L2[prow] = valid ? __ldg(&lse[row]) * 1.4426950408889634f : INFINITY;
+      if (L2 != nullptr) L2[prow] = valid ? -__ldg(&lse[row]) * 1.4426950408889634f : -INFINITY;
     }
     if (valid) {
       const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);

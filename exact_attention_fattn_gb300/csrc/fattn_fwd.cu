@@ -220,36 +220,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t o[32];
             tmem_ld32(tO + 32 * ch, o);
             tmem_ld_wait32(o);
+            const uint64_t a2 = splat2(alpha);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            for (int i = 0; i < 16; ++i) unpack2(fmul2(pack2(o[2 * i], o[2 * i + 1]), a2), o[2 * i], o[2 * i + 1]);
             tmem_st32(tO + 32 * ch, o);
           }
         }
       }
-      const float neg_m = -m_ref;
-      // Partial sums per 32-column group keep the additions independent.
-      float rs[4], rs_bf[4];
+      const uint64_t c2 = splat2(c);
+      const uint64_t nm2 = splat2(-m_ref);
+      // Two columns per instruction (packed fp32 pairs); partial sums per
+      // 32-column group keep the additions independent.
+      uint64_t rs2[4], rb2[4];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         uint32_t pk[16];
-        float e0 = 0.f, e1 = 0.f, b0 = 0.f, b1 = 0.f;
+        uint64_t e2 = 0ull, b2 = 0ull;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float a0 = ex2_approx(fmaf(__uint_as_float(sv[g][2 * i]), c, neg_m));
-          const float a1 = ex2_approx(fmaf(__uint_as_float(sv[g][2 * i + 1]), c, neg_m));
+          uint32_t x0, x1;
+          unpack2(ffma2(pack2(sv[g][2 * i], sv[g][2 * i + 1]), c2, nm2), x0, x1);
+          const float a0 = ex2_approx(__uint_as_float(x0));
+          const float a1 = ex2_approx(__uint_as_float(x1));
           pk[i] = pack_bf16x2(a0, a1);
-          e0 += a0;
-          e1 += a1;
+          e2 = fadd2(e2, pack2(__float_as_uint(a0), __float_as_uint(a1)));
           // O is divided by the sum of the bf16 values that P V actually
           // used, so that O is a convex combination of V rows with the
           // rounded weights (exact for a row dominated by one key); L keeps
           // the fp32 sum.
-          b0 += __uint_as_float(pk[i] << 16);
-          b1 += __uint_as_float(pk[i] & 0xffff0000u);
+          b2 = fadd2(b2, pack2(pk[i] << 16, pk[i] & 0xffff0000u));
         }
         tmem_st16(tP + 16 * g, pk);
-        rs[g] = e0 + e1;
-        rs_bf[g] = b0 + b1;
+        rs2[g] = e2;
+        rb2[g] = b2;
+      }
+      float rs[4], rs_bf[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint32_t u0, u1;
+        unpack2(rs2[g], u0, u1);
+        rs[g] = __uint_as_float(u0) + __uint_as_float(u1);
+        unpack2(rb2[g], u0, u1);
+        rs_bf[g] = __uint_as_float(u0) + __uint_as_float(u1);
       }
       l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
       l_bf += (rs_bf[0] + rs_bf[1]) + (rs_bf[2] + rs_bf[3]);

@@ -29,7 +29,7 @@ cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensor
                        cudaStream_t stream);
 
 struct BwdArgs {
-  const float* L2;            // [BH, Np]: lse * log2(e), +inf past N (Np = N rounded up to 128)
+  const float* L2;            // [BH, Np]: -lse * log2(e), -inf past N (Np = N rounded up to 128)
   const float* D;             // [BH, Np]: rowsum(dO o O), 0 past N
   float* dq_accum;            // [BH, N, d] fp32
   DeviceStatus* status;
@@ -40,7 +40,7 @@ struct BwdArgs {
   float scale_log2;
 };
 
-// D (and, when L2 != nullptr, L2 = lse * log2 e) in a [BH, pitch] layout with
+// D (and, when L2 != nullptr, L2 = -lse * log2 e) in a [BH, pitch] layout with
 // padding rows N..pitch-1; zeroes dq_accum [BH, N, d].
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, const float* lse, float* D,
                                   float* L2, float* dq_accum, int BH, int N, int pitch, int d,

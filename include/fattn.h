@@ -75,7 +75,7 @@ int fattn_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_accu
                          int B, int H, int N, int d, fattn_stream_t stream);
 
 /*
- * Workspace the backward pass needs, in bytes: D and L*log2(e) (fp32, each
+ * Workspace the backward pass needs, in bytes: D and -L*log2(e) (fp32, each
  * [B*H, Np] with Np = N rounded up to a multiple of 128), then the fp32 dQ
  * accumulator ([B,H,N,d]); each part starts on a 256-byte boundary.
  * Returns 0 for invalid sizes.
@@ -104,7 +104,7 @@ int fattn_bwd(const void* q, const void* k, const void* v, const void* o,
  * The three stages that fattn_bwd enqueues, exported for callers that time
  * or schedule them separately.  Run in this order on one workspace they do
  * exactly what fattn_bwd does:
- *   fattn_bwd_prepare: D = rowsum(dO o O) and L*log2(e) into the workspace,
+ *   fattn_bwd_prepare: D = rowsum(dO o O) and -L*log2(e) into the workspace,
  *                      and zero its fp32 dQ accumulator;
  *   fattn_bwd_main:    the recomputation kernel: writes dk, dv and adds the
  *                      dQ partial sums into the accumulator;
@@ -130,7 +130,7 @@ int fattn_bwd_finish(const void* workspace, size_t workspace_bytes, void* dq,
  *
  * The pages have no counterpart to this entry point; it is a service of the
  * library.  It does what fattn_bwd does, with the same arguments minus the
- * workspace, but takes its scratch (D, L*log2(e) and the fp32 dQ
+ * workspace, but takes its scratch (D, -L*log2(e) and the fp32 dQ
  * accumulator) from a fixed device array compiled into the library
  * (FATTN_NOALLOC_SCRATCH_BYTES, 64 MiB, held on every device that loads the
  * library until the process exits).  It is meant for code that has no way
