@@ -92,6 +92,22 @@ int make_map(CUtensorMap* m, const void* ptr, int N, int BH, int d, int box_rows
   return r == CUDA_SUCCESS ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
+// 3-D fp32 view {d, N, B*H} of the dQ accumulator: 32-column (128-byte) x
+// 32-row boxes, 128-byte swizzle.
+int make_acc_map(CUtensorMap* m, const void* ptr, int N, int BH, int d) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                                 static_cast<cuuint64_t>(N) * d * 4};
+  const cuuint32_t box[3] = {32u, 32u, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA; }
@@ -204,13 +220,14 @@ int bwd_main_impl(const void* q, const void* k, const void* v, const void* dO, v
   const BwdWorkspace ws = bwd_workspace(B, H, N, d);
   char* wbase = static_cast<char*>(workspace);
   int rc;
-  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv, tacc;
   if ((rc = make_map(&tq, q, N, BH, d, 128)) != FATTN_OK) return rc;
   if ((rc = make_map(&tk, k, N, BH, d, 128)) != FATTN_OK) return rc;
   if ((rc = make_map(&tv, v, N, BH, d, 128)) != FATTN_OK) return rc;
   if ((rc = make_map(&tdo, dO, N, BH, d, 128)) != FATTN_OK) return rc;
   if ((rc = make_map(&tdk, dk, N, BH, d, 32)) != FATTN_OK) return rc;
   if ((rc = make_map(&tdv, dv, N, BH, d, 32)) != FATTN_OK) return rc;
+  if ((rc = make_acc_map(&tacc, wbase + ws.acc_off, N, BH, d)) != FATTN_OK) return rc;
   BwdArgs a;
   a.L2 = reinterpret_cast<const float*>(wbase + ws.l2_off);
   a.D = reinterpret_cast<const float*>(wbase + ws.d_off);
@@ -224,7 +241,7 @@ int bwd_main_impl(const void* q, const void* k, const void* v, const void* dO, v
   a.BH = BH;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
-  return from_cuda(launch_bwd_main(d, causal != 0, tq, tk, tv, tdo, tdk, tdv, a, st));
+  return from_cuda(launch_bwd_main(d, causal != 0, tq, tk, tv, tdo, tdk, tdv, tacc, a, st));
 }
 
 int bwd_finish_impl(const void* workspace, void* dq, int B, int H, int N, int d, float scale,

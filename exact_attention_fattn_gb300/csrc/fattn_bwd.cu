@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-               const BwdArgs args) {
+               const __grid_constant__ CUtensorMap tm_dqacc, const BwdArgs args) {
   using C = BwdCfg<HD>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_do);
     tma_prefetch_desc(&tm_dk);
     tma_prefetch_desc(&tm_dv);
+    tma_prefetch_desc(&tm_dqacc);
   }
   tc_fence_before();
   __syncthreads();
@@ -238,35 +239,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(kBarDsFull));
-      // ---- dQ_i rows (TMEM lane = query row), this half's d/2 columns ->
-      // fp32 atomics, through a per-warp shared-memory transpose so that each
-      // atomic instruction covers four 128-byte row segments.
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDqFull), ph, wc, kWaitDqFull));
       if (!ok) break;
       tc_fence_after();
+      if constexpr (HD == 128) {
+        // ---- dQ^T (TMEM lane = head-dim index r, columns = query rows of
+        // this half): one fp32 reduce-add per query, 32 lanes = 128 bytes.
+        float* dst = args.dq_accum + static_cast<size_t>(bh) * N * HD + r;
 #pragma unroll 1
-      for (int ch = half * (HD / 64); ch < (half + 1) * (HD / 64); ++ch) {
-        uint32_t dq[32];
-        tmem_ld32(tB + 32 * ch, dq);
-        tmem_ld_wait32(dq);
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t dq[32];
+          tmem_ld32(tB + col0 + 32 * ch, dq);
+          tmem_ld_wait32(dq);
+          const int qb = q0 + col0 + 32 * ch;
+          if (qb + 32 <= N) {
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4)
-          st_shared_v4(stg + lane * 128 + (static_cast<uint32_t>(c4 ^ (lane & 7)) << 4),
-                       dq[4 * c4], dq[4 * c4 + 1], dq[4 * c4 + 2], dq[4 * c4 + 3]);
-        __syncwarp();
+            for (int c = 0; c < 32; ++c) red_add_f32(dst + static_cast<size_t>(qb + c) * HD, dq[c]);
+          } else {
 #pragma unroll
-        for (int k4 = 0; k4 < 8; ++k4) {
-          const int rl = k4 * 4 + (lane >> 3);
-          const int c4 = lane & 7;
-          const float4 v = *reinterpret_cast<const float4*>(
-              smem + C::kDsOff + warp * 4096 + rl * 128 + ((c4 ^ (rl & 7)) << 4));
-          const int q = q0 + wq * 32 + rl;
-          if (q < N)
-            atomicAdd(reinterpret_cast<float4*>(
-                          args.dq_accum + (static_cast<size_t>(bh) * N + q) * HD + ch * 32 + c4 * 4),
-                      v);
+            for (int c = 0; c < 32; ++c)
+              if (qb + c < N) red_add_f32(dst + static_cast<size_t>(qb + c) * HD, dq[c]);
+          }
         }
-        __syncwarp();
+      } else {
+        // ---- dQ_i rows (TMEM lane = query row), this half's d/2 columns, in
+        // 32-column chunks: TMEM -> swizzled shared memory (per warp, 32 rows
+        // x 128 bytes) -> one TMA tensor reduce-add into the accumulator.
+#pragma unroll 1
+        for (int ch = half * (HD / 64); ch < (half + 1) * (HD / 64); ++ch) {
+          uint32_t dq[32];
+          tmem_ld32(tB + 32 * ch, dq);
+          tmem_ld_wait32(dq);
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4)
+            st_shared_v4(stg + lane * 128 + (static_cast<uint32_t>(c4 ^ (lane & 7)) << 4),
+                         dq[4 * c4], dq[4 * c4 + 1], dq[4 * c4 + 2], dq[4 * c4 + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && q0 + wq * 32 < N) {
+            tma_reduce_add_3d(&tm_dqacc, stg, ch * 32, q0 + wq * 32, bh);
+            bulk_commit_group();
+            bulk_wait_group_read0();   // the staging buffer is reused next
+          }
+          __syncwarp();
+        }
       }
       tc_fence_before();
       mbar_arrive(bar(kBarDqEmpty));
@@ -361,15 +377,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_warp(bar(kBarDsFull), ph, wc, kWaitDsFull)) goto mma_end;
         tc_fence_after();
         mma_tmem_a(tmem + C::kColDK, kColB, sQ(s), acc);         // dK += dS^T Q
-        // dQ = dS K into B (dS^T there has just been consumed by the dK MMA,
-        // issued before): A = dS (q contiguous, MN-major), B = K (HD contiguous).
+        // dQ into B (dS^T there has just been consumed by the dK MMA, issued
+        // before).  d = 128: dQ^T = K^T dS^T, A = K (d contiguous, MN-major),
+        // B = dS (q contiguous, MN-major).  d = 64: dQ = dS K, the same two
+        // operands in the other order.
         {
-          const uint64_t da = sdesc_sw128(sDs, 16384, 1024);
-          const uint64_t db = sdesc_sw128(sK, C::kChunkBytes, 1024);
+          const uint64_t dds = sdesc_sw128(sDs, 16384, 1024);
+          const uint64_t dk = sdesc_sw128(sK, C::kChunkBytes, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ss_w(tmem + kColB, da + ((kk * 2048) >> 4), db + ((kk * 2048) >> 4), idesc_mm,
-                     kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint32_t off = (kk * 2048) >> 4;
+            if constexpr (HD == 128)
+              mma_ss_w(tmem + kColB, dk + off, dds + off, idesc_mm, kk > 0 ? 1u : 0u);
+            else
+              mma_ss_w(tmem + kColB, dds + off, dk + off, idesc_mm, kk > 0 ? 1u : 0u);
+          }
         }
         mma_commit_w(bar(kBarDqFull));
         mma_commit_w(bar(kBarQEmpty + s));
@@ -438,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int HD, bool CAUSAL>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                         const BwdArgs& a, cudaStream_t stream) {
+                         const CUtensorMap& tacc, const BwdArgs& a, cudaStream_t stream) {
   using C = BwdCfg<HD>;
   auto kern = bwd_kernel<HD, CAUSAL>;
   cudaError_t e =
@@ -446,7 +468,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   if (e != cudaSuccess) return e;
   const int n_tiles = (a.N + kTile - 1) / kTile;
   const dim3 grid(static_cast<unsigned>(n_tiles * a.BH));
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdk, tdv, a);
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdk, tdv, tacc, a);
   return cudaGetLastError();
 }
 
@@ -454,14 +476,14 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 cudaError_t launch_bwd_main(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
-                            const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdArgs& a,
-                            cudaStream_t stream) {
+                            const CUtensorMap& tdk, const CUtensorMap& tdv,
+                            const CUtensorMap& tacc, const BwdArgs& a, cudaStream_t stream) {
   if (d == 64) {
-    return causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, tdk, tdv, a, stream)
-                  : launch_bwd_t<64, false>(tq, tk, tv, tdo, tdk, tdv, a, stream);
+    return causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, tdk, tdv, tacc, a, stream)
+                  : launch_bwd_t<64, false>(tq, tk, tv, tdo, tdk, tdv, tacc, a, stream);
   }
-  return causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, tdk, tdv, a, stream)
-                : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdk, tdv, a, stream);
+  return causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, tdk, tdv, tacc, a, stream)
+                : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdk, tdv, tacc, a, stream);
 }
 
 }  // namespace fattn

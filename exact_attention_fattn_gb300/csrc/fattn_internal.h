@@ -46,10 +46,12 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dO, const float* ls
                                   float* L2, float* dq_accum, int BH, int N, int pitch, int d,
                                   cudaStream_t stream);
 
+// tacc: 3-D fp32 view {d, N, B*H} of the dQ accumulator, 32 x 32 boxes,
+// 128-byte swizzle (the target of the dQ reduce-adds).
 cudaError_t launch_bwd_main(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
-                            const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdArgs& a,
-                            cudaStream_t stream);
+                            const CUtensorMap& tdk, const CUtensorMap& tdv,
+                            const CUtensorMap& tacc, const BwdArgs& a, cudaStream_t stream);
 
 cudaError_t launch_dq_convert(const float* dq_accum, void* dq, long long elems, float scale,
                               cudaStream_t stream);

@@ -139,6 +139,18 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int
       : "memory");
 }
 
+// Element-wise add of a shared-memory box into global memory through a
+// tensor map (fp32 here): global[box] += shared[box].  Out-of-range rows of
+// the box are skipped.
+__device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src, int c0, int c1,
+                                                  int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -158,6 +170,12 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, 
       "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
       "r"(ssrc), "r"(bytes)
       : "memory");
+}
+
+// global += v (fp32), no return value.
+__device__ __forceinline__ void red_add_f32(float* gaddr, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(gaddr), "f"(__uint_as_float(v))
+               : "memory");
 }
 
 // Make generic-proxy shared-memory writes visible to the async proxy (TMA).
