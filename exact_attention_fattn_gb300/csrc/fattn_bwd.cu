@@ -8,14 +8,24 @@
 //   dP^T = V_j dO_i^T                   (tcgen05)
 //   dS^T = P^T o (dP^T - D_i)           (bf16 to TMEM and, as dS, to shared memory)
 //   dV_j += P^T dO_i,  dK_j += dS^T Q_i (tcgen05, accumulators in TMEM)
-//   dQ_i  = dS K_j                      (tcgen05) -> fp32 atomics into dq_accum
+//   dQ_i  = dS K_j                      (tcgen05) -> fp32 reduce-adds into dq_accum
 // At the end dK_j * scale and dV_j are stored as bf16.  dQ = scale * dq_accum
 // is converted by a separate kernel.  The dQ and dK formulas follow from
 // S = scale Q K^T by the chain rule (the pages stop at dS).
 //
+// The global reduce-adds of dQ are capped per SM (about 25 bytes/cycle
+// measured on GB300, whatever the path), so a 64 KiB dQ tile costs ~2600
+// cycles, as long as all five MMAs of the step.  They are therefore taken off
+// the critical path: the compute warps park the fp32 dQ tile in the Q/dO
+// shared-memory stage that the step has just finished with (64 KiB at d = 128,
+// 32 KiB at d = 64: exactly a dQ tile), in the 32 x 32 swizzled boxes of the
+// accumulator's tensor map, and go on; a reduce warp streams the boxes out
+// with TMA reduce-adds and only then hands the stage back to the loader.
+//
 // Warps: 0-7 compute, as two warpgroups that split the 128 query columns of
 // every key row (P and dS are elementwise, so the halves never exchange
-// anything); 8 TMEM allocation + MMA issue; 9 TMA producer; 10-11 idle.
+// anything); 8 TMEM allocation + MMA issue; 9 TMA producer; 10 dQ reduce;
+// 11 idle.
 // TMEM (512 columns): A [0,128) holds S^T, then P^T; B [128,256) holds dP^T,
 // then dS^T, then dQ ([128,128+d)).  Each warpgroup packs its 64 bf16 values
 // (32 columns) into the first half of the 64 fp32 columns it read itself
@@ -35,6 +45,7 @@ constexpr int kThreads = 384;
 constexpr int kComputeThreads = 256;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
+constexpr int kReduceWarp = 10;
 constexpr uint32_t kColA = 0, kColB = 128, kColDV = 256;
 
 template <int HD>
@@ -149,7 +160,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tB = tmem + lane_off + kColB;
     const uint64_t c2 = splat2(args.scale_log2);
     const uint32_t ds_base = sbase + C::kDsOff;
-    const uint32_t stg = ds_base + warp * 4096;  // per-warp staging for dQ rows
     const int col0 = 64 * half;
     bool ok = true;
     for (int it = 0; it < n_it && ok; ++it) {
@@ -239,50 +249,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(kBarDsFull));
+      // ---- dQ_i rows (TMEM lane = query row), this half's d/2 columns ->
+      // the Q/dO stage of this step (free now: every MMA that read it has
+      // completed), as 32 x 32 fp32 boxes with the 128-byte swizzle.
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDqFull), ph, wc, kWaitDqFull));
       if (!ok) break;
       tc_fence_after();
-      if constexpr (HD == 128) {
-        // ---- dQ^T (TMEM lane = head-dim index r, columns = query rows of
-        // this half): one fp32 reduce-add per query, 32 lanes = 128 bytes.
-        float* dst = args.dq_accum + static_cast<size_t>(bh) * N * HD + r;
-#pragma unroll 1
-        for (int ch = 0; ch < 2; ++ch) {
-          uint32_t dq[32];
-          tmem_ld32(tB + col0 + 32 * ch, dq);
-          tmem_ld_wait32(dq);
-          const int qb = q0 + col0 + 32 * ch;
-          if (qb + 32 <= N) {
+      {
+        const uint32_t stage = sbase + C::kStageOff + s * C::kStageBytes;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) red_add_f32(dst + static_cast<size_t>(qb + c) * HD, dq[c]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-              if (qb + c < N) red_add_f32(dst + static_cast<size_t>(qb + c) * HD, dq[c]);
-          }
-        }
-      } else {
-        // ---- dQ_i rows (TMEM lane = query row), this half's d/2 columns, in
-        // 32-column chunks: TMEM -> swizzled shared memory (per warp, 32 rows
-        // x 128 bytes) -> one TMA tensor reduce-add into the accumulator.
-#pragma unroll 1
         for (int ch = half * (HD / 64); ch < (half + 1) * (HD / 64); ++ch) {
           uint32_t dq[32];
           tmem_ld32(tB + 32 * ch, dq);
           tmem_ld_wait32(dq);
+          const uint32_t box = stage + (wq * (HD / 32) + ch) * 4096;
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4)
-            st_shared_v4(stg + lane * 128 + (static_cast<uint32_t>(c4 ^ (lane & 7)) << 4),
+            st_shared_v4(box + lane * 128 + (static_cast<uint32_t>(c4 ^ (lane & 7)) << 4),
                          dq[4 * c4], dq[4 * c4 + 1], dq[4 * c4 + 2], dq[4 * c4 + 3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0 && q0 + wq * 32 < N) {
-            tma_reduce_add_3d(&tm_dqacc, stg, ch * 32, q0 + wq * 32, bh);
-            bulk_commit_group();
-            bulk_wait_group_read0();   // the staging buffer is reused next
-          }
-          __syncwarp();
         }
+        fence_proxy_async_smem();
       }
       tc_fence_before();
       mbar_arrive(bar(kBarDqEmpty));
@@ -377,24 +363,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_warp(bar(kBarDsFull), ph, wc, kWaitDsFull)) goto mma_end;
         tc_fence_after();
         mma_tmem_a(tmem + C::kColDK, kColB, sQ(s), acc);         // dK += dS^T Q
-        // dQ into B (dS^T there has just been consumed by the dK MMA, issued
-        // before).  d = 128: dQ^T = K^T dS^T, A = K (d contiguous, MN-major),
-        // B = dS (q contiguous, MN-major).  d = 64: dQ = dS K, the same two
-        // operands in the other order.
+        // dQ = dS K into B (dS^T there has just been consumed by the dK MMA,
+        // issued before): A = dS (q contiguous, MN-major), B = K (HD contiguous).
         {
           const uint64_t dds = sdesc_sw128(sDs, 16384, 1024);
           const uint64_t dk = sdesc_sw128(sK, C::kChunkBytes, 1024);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
             const uint32_t off = (kk * 2048) >> 4;
-            if constexpr (HD == 128)
-              mma_ss_w(tmem + kColB, dk + off, dds + off, idesc_mm, kk > 0 ? 1u : 0u);
-            else
-              mma_ss_w(tmem + kColB, dds + off, dk + off, idesc_mm, kk > 0 ? 1u : 0u);
+            mma_ss_w(tmem + kColB, dds + off, dk + off, idesc_mm, kk > 0 ? 1u : 0u);
           }
         }
         mma_commit_w(bar(kBarDqFull));
-        mma_commit_w(bar(kBarQEmpty + s));
         if (it + 1 < n_it) {
           if (!qfull(it + 1)) goto mma_end;
           tc_fence_after();
@@ -446,6 +426,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(bar(kBarQFull + (it & 1)), (it >> 1) & 1, args.wait_budget);
       mbar_wait_drain(bar(kBarKv), 0, args.wait_budget);
     }
+    __syncwarp();
+  }
+
+  if (warp == kReduceWarp) {
+    // ================================================================ dQ reduce
+    // For each step: once the compute warps have parked dQ_i in stage s,
+    // reduce-add its boxes into the accumulator, wait until the TMA engine
+    // has read them, and hand the stage back to the loader.
+    bool ok = true;
+    for (int it = 0; it < n_it && ok; ++it) {
+      const int s = it & 1;
+      const int q0 = (i0 + it) * kTile;
+      ok = mbar_wait_warp(bar(kBarDqEmpty), it & 1, wc, kWaitDqEmpty);
+      if (!ok) break;
+      if (lane == 0) {
+        const uint32_t stage = sbase + C::kStageOff + s * C::kStageBytes;
+        for (int qb = 0; qb < 4; ++qb) {
+          if (q0 + qb * 32 >= N) break;
+#pragma unroll
+          for (int ch = 0; ch < HD / 32; ++ch)
+            tma_reduce_add_3d(&tm_dqacc, stage + (qb * (HD / 32) + ch) * 4096, ch * 32,
+                              q0 + qb * 32, bh);
+        }
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(bar(kBarQEmpty + s));
+      }
+      __syncwarp();
+    }
+    if (lane == 0) bulk_wait_group0();
     __syncwarp();
   }
 
