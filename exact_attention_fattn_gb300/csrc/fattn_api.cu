@@ -130,12 +130,12 @@ int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, 
   DeviceStatus* status = nullptr;
   if ((rc = device_setup(&status)) != FATTN_OK) return rc;
   const int BH = B * H;
-  CUtensorMap tq, tk, tv, to;
+  CUtensorMap tq, tk, tv;
   if ((rc = make_map(&tq, q, N, BH, d, 128)) != FATTN_OK) return rc;
   if ((rc = make_map(&tk, k, N, BH, d, 128)) != FATTN_OK) return rc;
   if ((rc = make_map(&tv, v, N, BH, d, 128)) != FATTN_OK) return rc;
-  if ((rc = make_map(&to, o, N, BH, d, 32)) != FATTN_OK) return rc;
   FwdArgs a;
+  a.o = static_cast<uint16_t*>(o);
   a.lse = lse;
   a.status = status;
   a.N = N;
@@ -146,7 +146,7 @@ int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, 
     a.wait_budget = g_budget;
     a.tau_log2 = g_tau_log2;
   }
-  return from_cuda(launch_fwd(d, causal != 0, tq, tk, tv, to, a,
+  return from_cuda(launch_fwd(d, causal != 0, tq, tk, tv, a,
                               reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -12,6 +12,7 @@ struct DeviceStatus;
 
 // Everything a forward launch needs besides the tensor maps.
 struct FwdArgs {
+  uint16_t* o;                // bf16 [BH, N, d]
   float* lse;                 // [BH, N]
   DeviceStatus* status;
   long long wait_budget;      // cycles
@@ -22,11 +23,9 @@ struct FwdArgs {
 };
 
 // Launch the forward kernel for head dim d (64/128).  Tensor maps are 3-D
-// {d, N, B*H} views with a 128-byte swizzle: q/k/v with 128-row boxes, o with
-// 32-row boxes.
+// {d, N, B*H} views of q, k, v with 128-row boxes and a 128-byte swizzle.
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a,
-                       cudaStream_t stream);
+                       const CUtensorMap& tv, const FwdArgs& a, cudaStream_t stream);
 
 struct BwdArgs {
   const float* L2;            // [BH, Np]: -lse * log2(e), -inf past N (Np = N rounded up to 128)
