@@ -186,7 +186,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = qs + r_tile;
       float m_ref = -INFINITY;  // running reference max, log2 units
       float l = 0.f;            // sum of the fp32 probabilities (gives L)
-      float l_bf = 0.f;         // sum of their bf16 roundings (normalises O)
+      // Sum, over the tiles, of the bf16 rounding error of the probability
+      // of each tile's largest score.  P V uses bf16 probabilities while l
+      // sums fp32 ones; for a row dominated by one key that mismatch alone
+      // would leave O off by up to 2^-9 |v|, so O is normalised by l + l_fix,
+      // which is exact for the dominating key.  (The other keys' rounding
+      // errors stay, each weighted by its own small share of the row.)
+      float l_fix = 0.f;
       for (int j = 0; j < nj; ++j) {
         ok = __all_sync(0xffffffffu, mbar_wait(b.s_full[t], s_count & 1, wc, kWaitSFull));
         if (!ok) break;
@@ -240,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
           if (need) m_ref = m_new;
           l *= alpha;
-          l_bf *= alpha;
+          l_fix *= alpha;
           if (j > 0) {
 #pragma unroll 1
             for (int ch = 0; ch < HD / 32; ++ch) {
@@ -255,15 +261,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        {
+          // the same arithmetic as the element loop below, for the largest score
+          const float p_top = ex2_approx(fmaf(mx, c, -m_ref));
+          l_fix += __bfloat162float(__float2bfloat16_rn(p_top)) - p_top;
+        }
         const uint64_t c2 = splat2(c);
         const uint64_t nm2 = splat2(-m_ref);
         // Two columns per instruction (packed fp32 pairs); partial sums per
         // 32-column group keep the additions independent.
-        uint64_t rs2[4], rb2[4];
+        uint64_t rs2[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           uint32_t pk[16];
-          uint64_t e2 = 0ull, b2 = 0ull;
+          uint64_t e2 = 0ull;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             uint32_t x0, x1;
@@ -272,27 +283,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float a1 = ex2_approx(__uint_as_float(x1));
             pk[i] = pack_bf16x2(a0, a1);
             e2 = fadd2(e2, pack2(__float_as_uint(a0), __float_as_uint(a1)));
-            // O is divided by the sum of the bf16 values that P V actually
-            // used, so that O is a convex combination of V rows with the
-            // rounded weights (exact for a row dominated by one key); L
-            // keeps the fp32 sum.
-            b2 = fadd2(b2, pack2(pk[i] << 16, pk[i] & 0xffff0000u));
           }
           tmem_st16(tP + 16 * g, pk);
           rs2[g] = e2;
-          rb2[g] = b2;
         }
-        float rs[4], rs_bf[4];
+        float rs[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           uint32_t u0, u1;
           unpack2(rs2[g], u0, u1);
           rs[g] = __uint_as_float(u0) + __uint_as_float(u1);
-          unpack2(rb2[g], u0, u1);
-          rs_bf[g] = __uint_as_float(u0) + __uint_as_float(u1);
         }
         l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-        l_bf += (rs_bf[0] + rs_bf[1]) + (rs_bf[2] + rs_bf[3]);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(b.p_full[t]);
@@ -305,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ++o_count;
       tc_fence_after();
-      const float inv = 1.f / l_bf;
+      const float inv = 1.f / (l + l_fix);
       const bool row_ok = row < N;
       uint4* orow = reinterpret_cast<uint4*>(args.o + (static_cast<size_t>(w.bh) * N +
                                                        (row_ok ? row : 0)) * HD);
