@@ -61,7 +61,7 @@ struct BwdCfg {
   static constexpr int kDsBytes = kTile * kTile * 2;
   static constexpr int kLdOff = kDsOff + kDsBytes;  // stage s: L2[128], D[128]
   static constexpr int kBarOff = kLdOff + 2 * 1024;
-  static constexpr int kNumBars = 13;
+  static constexpr int kNumBars = 17;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16;
   static constexpr uint32_t kColDK = kColDV + HD;
@@ -71,8 +71,8 @@ struct BwdCfg {
 // Barrier indices.
 enum : int {
   kBarKv = 0,
-  kBarQFull = 1,   // +stage
-  kBarQEmpty = 3,  // +stage
+  kBarQFull = 1,   // +stage: Q_i and the L / D vectors landed
+  kBarQEmpty = 3,  // +stage: Q_i's half of the stage is free again
   kBarSFull = 5,
   kBarDpFull = 6,
   kBarPFull = 7,
@@ -81,6 +81,8 @@ enum : int {
   kBarDqEmpty = 10,
   kBarDkvFull = 11,
   kBarMmaDone = 12,
+  kBarDoFull = 13,   // +stage: dO_i landed
+  kBarDoEmpty = 15,  // +stage: dO_i's half of the stage is free again
 };
 
 template <int HD, bool CAUSAL>
@@ -117,6 +119,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kBarQFull + s), 1);
       mbar_init(bar(kBarQEmpty + s), 1);
+      mbar_init(bar(kBarDoFull + s), 1);
+      mbar_init(bar(kBarDoEmpty + s), 1);
     }
     mbar_init(bar(kBarSFull), 1);
     mbar_init(bar(kBarDpFull), 1);
@@ -346,11 +350,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto qfull = [&](int it) {
         return mbar_wait_warp(bar(kBarQFull + (it & 1)), (it >> 1) & 1, wc, kWaitKvFull);
       };
+      auto dofull = [&](int it) {
+        return mbar_wait_warp(bar(kBarDoFull + (it & 1)), (it >> 1) & 1, wc, kWaitKvFull);
+      };
       if (!mbar_wait_warp(bar(kBarKv), 0, wc, kWaitKvFull)) goto mma_end;
       if (!qfull(0)) goto mma_end;
       tc_fence_after();
       mma_kmajor(tmem + kColA, sK, sQ(0));   // S^T
       mma_commit_w(bar(kBarSFull));
+      if (!dofull(0)) goto mma_end;
+      tc_fence_after();
       mma_kmajor(tmem + kColB, sV, sDo(0));  // dP^T
       mma_commit_w(bar(kBarDpFull));
       for (int it = 0; it < n_it; ++it) {
@@ -381,6 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_kmajor(tmem + kColA, sK, sQ(s ^ 1));               // S^T (next), overlaps the dQ read-out
           mma_commit_w(bar(kBarSFull));
           if (!mbar_wait_warp(bar(kBarDqEmpty), ph, wc, kWaitDqEmpty)) goto mma_end;
+          if (!dofull(it + 1)) goto mma_end;
           tc_fence_after();
           mma_kmajor(tmem + kColB, sV, sDo(s ^ 1));              // dP^T (next)
           mma_commit_w(bar(kBarDpFull));
@@ -403,27 +413,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d_w(sbase + C::kVOff + cc * C::kChunkBytes, &tm_v, bar(kBarKv), cc * 64, kv0,
                       bh);
       }
-      int issued = 0;
+      // Each stage is refilled in two halves, as the reduce warp frees them:
+      // Q_i with the L / D vectors (needed first, by S^T), then dO_i.
+      int issued_q = 0, issued_do = 0;
       for (int it = 0; it < n_it; ++it) {
         const int s = it & 1;
         const int rnd = it >> 1;
-        if (rnd > 0 && !mbar_wait_warp(bar(kBarQEmpty + s), (rnd - 1) & 1, wc, kWaitKvEmpty))
-          break;
-        const uint32_t full = bar(kBarQFull + s);
-        mbar_arrive_expect_tx_w(full, 2 * C::kTileBytes + 1024);
         const int q0 = (i0 + it) * kTile;
         const uint32_t dst = sbase + C::kStageOff + s * C::kStageBytes;
-        for (int cc = 0; cc < C::kChunks; ++cc) {
-          tma_load_3d_w(dst + cc * C::kChunkBytes, &tm_q, full, cc * 64, q0, bh);
-          tma_load_3d_w(dst + C::kTileBytes + cc * C::kChunkBytes, &tm_do, full, cc * 64, q0, bh);
-        }
+        if (rnd > 0 && !mbar_wait_warp(bar(kBarQEmpty + s), (rnd - 1) & 1, wc, kWaitKvEmpty))
+          break;
+        const uint32_t qf = bar(kBarQFull + s);
+        mbar_arrive_expect_tx_w(qf, C::kTileBytes + 1024);
+        for (int cc = 0; cc < C::kChunks; ++cc)
+          tma_load_3d_w(dst + cc * C::kChunkBytes, &tm_q, qf, cc * 64, q0, bh);
         const size_t vec = static_cast<size_t>(bh) * pitch + q0;
-        bulk_load_1d_w(sbase + C::kLdOff + s * 1024, args.L2 + vec, 512, full);
-        bulk_load_1d_w(sbase + C::kLdOff + s * 1024 + 512, args.D + vec, 512, full);
-        issued = it + 1;
+        bulk_load_1d_w(sbase + C::kLdOff + s * 1024, args.L2 + vec, 512, qf);
+        bulk_load_1d_w(sbase + C::kLdOff + s * 1024 + 512, args.D + vec, 512, qf);
+        issued_q = it + 1;
+        if (rnd > 0 && !mbar_wait_warp(bar(kBarDoEmpty + s), (rnd - 1) & 1, wc, kWaitKvEmpty))
+          break;
+        const uint32_t df = bar(kBarDoFull + s);
+        mbar_arrive_expect_tx_w(df, C::kTileBytes);
+        for (int cc = 0; cc < C::kChunks; ++cc)
+          tma_load_3d_w(dst + C::kTileBytes + cc * C::kChunkBytes, &tm_do, df, cc * 64, q0, bh);
+        issued_do = it + 1;
       }
-      for (int it = max(0, issued - 2); it < issued; ++it)
+      for (int it = max(0, issued_q - 2); it < issued_q; ++it)
         mbar_wait_drain(bar(kBarQFull + (it & 1)), (it >> 1) & 1, args.wait_budget);
+      for (int it = max(0, issued_do - 2); it < issued_do; ++it)
+        mbar_wait_drain(bar(kBarDoFull + (it & 1)), (it >> 1) & 1, args.wait_budget);
       mbar_wait_drain(bar(kBarKv), 0, args.wait_budget);
     }
     __syncwarp();
@@ -432,8 +451,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kReduceWarp) {
     // ================================================================ dQ reduce
     // For each step: once the compute warps have parked dQ_i in stage s,
-    // reduce-add its boxes into the accumulator, wait until the TMA engine
-    // has read them, and hand the stage back to the loader.
+    // reduce-add its boxes into the accumulator in two groups -- query rows
+    // 0-63 sit in the stage's Q half, rows 64-127 in its dO half -- and hand
+    // each half back to the loader as soon as the TMA engine has read it.
     bool ok = true;
     for (int it = 0; it < n_it && ok; ++it) {
       const int s = it & 1;
@@ -442,16 +462,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (lane == 0) {
         const uint32_t stage = sbase + C::kStageOff + s * C::kStageBytes;
-        for (int qb = 0; qb < 4; ++qb) {
-          if (q0 + qb * 32 >= N) break;
+        for (int half = 0; half < 2; ++half) {
+          for (int qb = 2 * half; qb < 2 * half + 2; ++qb) {
+            if (q0 + qb * 32 >= N) break;
 #pragma unroll
-          for (int ch = 0; ch < HD / 32; ++ch)
-            tma_reduce_add_3d(&tm_dqacc, stage + (qb * (HD / 32) + ch) * 4096, ch * 32,
-                              q0 + qb * 32, bh);
+            for (int ch = 0; ch < HD / 32; ++ch)
+              tma_reduce_add_3d(&tm_dqacc, stage + (qb * (HD / 32) + ch) * 4096, ch * 32,
+                                q0 + qb * 32, bh);
+          }
+          bulk_commit_group();
         }
-        bulk_commit_group();
-        bulk_wait_group_read0();
+        bulk_wait_group_read1();
         mbar_arrive(bar(kBarQEmpty + s));
+        bulk_wait_group_read0();
+        mbar_arrive(bar(kBarDoEmpty + s));
       }
       __syncwarp();
     }
