@@ -140,6 +140,43 @@ class ClockSampler:
                 "samples": len(inside), "window": window}
 
 
+# ---------------------------------------------------------------- replicas
+# Every rank runs an independent replica of the workload (attention over
+# (batch, head) needs no exchange); these helpers are the only cross-rank
+# steps, and they work with either the nccl (GPU) or the gloo (CPU) backend.
+
+def rank_info():
+    """(rank, world size, local rank) from the torchrun environment."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def replica_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own batch of the same workload."""
+    return base_seed + 7919 * rank
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """The slowest rank's time defines the step (whole-job timing)."""
+    if dist is None:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_replica: float, world: int, seconds: float) -> float:
+    """Units processed by all replicas per second."""
+    return world * units_per_replica / seconds
+
+
 def cpu_baseline(w, heads: int):
     """The fp64 oracle, as it stands, on `heads` (b, h) slices of the
     workload: full forward + backward of each slice on the host cores."""
@@ -213,9 +250,7 @@ def run_fattn(args, w):
     from exact_attention_fattn_gb300 import attention as A
     from exact_attention_fattn_gb300 import workloads as W
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, world, local = rank_info()
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -226,7 +261,7 @@ def run_fattn(args, w):
     torch.cuda.set_device(dev)
 
     # replicas only: each rank draws its own batch of the same workload
-    inp = W.make_inputs(w, seed=w.seed + 7919 * rank)
+    inp = W.make_inputs(w, seed=replica_seed(w.seed, rank))
     q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
@@ -265,8 +300,7 @@ def run_fattn(args, w):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
           for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
+    barrier(dist)
     torch.cuda.synchronize(dev)
     t_host0 = time.time()
     start.record(stream)
@@ -278,13 +312,8 @@ def run_fattn(args, w):
     end.record(stream)
     torch.cuda.synchronize(dev)
     t_host1 = time.time()
-    if dist is not None:
-        dist.barrier()
-    total_ms = start.elapsed_time(end)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    barrier(dist)
+    total_ms = max_over_ranks(start.elapsed_time(end), dist, dev)
     status = A.fattn_check_status(dev)
     if status != 0:
         raise RuntimeError(f"libfattn reported status {status} in the timed region")
@@ -317,21 +346,16 @@ def run_fattn(args, w):
         for _ in range(3):
             e2e_step()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if dist is not None:
-            dist.barrier()
+        barrier(dist)
         torch.cuda.synchronize(dev)
         e0.record(stream)
         for _ in range(e2e_steps):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = e0.elapsed_time(e1) / e2e_steps
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
         base, bwd = flop_counts(w)
-        e2e = {"value": world * (base + bwd) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": whole_job_rate(base + bwd, world, e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "steps": e2e_steps}
         if A.fattn_check_status(dev) != 0:
@@ -345,7 +369,7 @@ def run_fattn(args, w):
     peaks = load_peaks()
     base, bwd = flop_counts(w)
     ms_step = total_ms / args.steps
-    value = world * (base + bwd) / (ms_step * 1e-3) / 1e12
+    value = whole_job_rate(base + bwd, world, ms_step * 1e-3) / 1e12
     stage_flops = {"fwd": base, "bwd_main": bwd}
     dominant = max(per_stage, key=per_stage.get)
     dom_ms = per_stage[dominant]
