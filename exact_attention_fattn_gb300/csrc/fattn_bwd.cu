@@ -185,6 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       reg_fence32(p1);
       uint32_t* pv[2] = {p0, p1};
       const bool diag = CAUSAL && q0 == kv0;
+      // Only the diagonal tile and a K/V tile that runs past N need masks
+      // (warp-uniform test); padded query columns already get exponent -inf.
+      const bool need_mask = diag || kv0 + kTile > N;
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
 #pragma unroll
@@ -195,11 +198,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           unpack2(ffma2(pack2(pv[g][e], pv[g][e + 1]), c2, pack2(l4.x, l4.y)), x[0], x[1]);
           unpack2(ffma2(pack2(pv[g][e + 2], pv[g][e + 3]), c2, pack2(l4.z, l4.w)), x[2], x[3]);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int col = col0 + g * 32 + e + u;
-            float p = ex2_approx(__uint_as_float(x[u]));
-            if (!kv_valid || (diag && col < r)) p = 0.f;
-            pv[g][e + u] = __float_as_uint(p);
+          for (int u = 0; u < 4; ++u) pv[g][e + u] = __float_as_uint(ex2_approx(__uint_as_float(x[u])));
+        }
+        if (need_mask) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int col = col0 + g * 32 + e;
+            if (!kv_valid || (diag && col < r)) pv[g][e] = 0u;
           }
         }
         uint32_t pk[16];
