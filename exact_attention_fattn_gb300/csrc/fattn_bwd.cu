@@ -456,9 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kReduceWarp) {
     // ================================================================ dQ reduce
     // For each step: once the compute warps have parked dQ_i in stage s,
-    // reduce-add its boxes into the accumulator in two groups -- query rows
-    // 0-63 sit in the stage's Q half, rows 64-127 in its dO half -- and hand
-    // each half back to the loader as soon as the TMA engine has read it.
+    // reduce-add its boxes into the accumulator -- query rows 0-63 sit in the
+    // stage's Q half, rows 64-127 in its dO half -- and hand each half back
+    // to the loader as soon as the TMA engine has read it.
     bool ok = true;
     for (int it = 0; it < n_it && ok; ++it) {
       const int s = it & 1;
@@ -466,21 +466,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait_warp(bar(kBarDqEmpty), it & 1, wc, kWaitDqEmpty);
       if (!ok) break;
       if (lane == 0) {
+        // 8 KiB groups (two boxes), at most two in flight: the TMA engine
+        // serves the stage's loads in between instead of behind a whole
+        // 64 KiB reduce that drains at the per-SM reduce-add rate.
         const uint32_t stage = sbase + C::kStageOff + s * C::kStageBytes;
-        for (int half = 0; half < 2; ++half) {
-          for (int qb = 2 * half; qb < 2 * half + 2; ++qb) {
-            if (q0 + qb * 32 >= N) break;
+        for (int qb = 0; qb < 4; ++qb) {
 #pragma unroll
-            for (int ch = 0; ch < HD / 32; ++ch)
+          for (int ch = 0; ch < HD / 32; ch += 2) {
+            if (q0 + qb * 32 < N) {
               tma_reduce_add_3d(&tm_dqacc, stage + (qb * (HD / 32) + ch) * 4096, ch * 32,
                                 q0 + qb * 32, bh);
+              tma_reduce_add_3d(&tm_dqacc, stage + (qb * (HD / 32) + ch + 1) * 4096,
+                                (ch + 1) * 32, q0 + qb * 32, bh);
+            }
+            bulk_commit_group();
+            bulk_wait_group_read1();
           }
-          bulk_commit_group();
+          if (qb == 1) {
+            bulk_wait_group_read0();
+            mbar_arrive(bar(kBarQEmpty + s));   // rows 0-63 (the Q half) read
+          }
         }
-        bulk_wait_group_read1();
-        mbar_arrive(bar(kBarQEmpty + s));
         bulk_wait_group_read0();
-        mbar_arrive(bar(kBarDoEmpty + s));
+        mbar_arrive(bar(kBarDoEmpty + s));      // rows 64-127 (the dO half) read
       }
       __syncwarp();
     }
