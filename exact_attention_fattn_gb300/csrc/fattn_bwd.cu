@@ -1,17 +1,25 @@
 // Main backward kernel of exact attention on sm_103a.
 //
-// Recomputation backward ("6.1 FlashAttention V1详解" §6.1-6.2): one CTA owns
-// a 128-row K/V tile j of one (batch, head) and walks the 128-row Q tiles i
-// (i >= j when causal).  Per step, with the kv rows on TMEM lanes:
+// Recomputation backward ("6.1 FlashAttention V1详解" §6.1-6.2): a work item
+// is a 128-row K/V tile j of one (batch, head); it walks the 128-row Q tiles
+// i (i >= j when causal).  Per step, with the kv rows on TMEM lanes:
 //   S^T  = K_j Q_i^T                    (tcgen05, fp32 in TMEM)
 //   P^T  = 2^(S^T*scale*log2e - L_i*log2e)    (one thread per kv row and query half; bf16 back to TMEM)
 //   dP^T = V_j dO_i^T                   (tcgen05)
 //   dS^T = P^T o (dP^T - D_i)           (bf16 to TMEM and, as dS, to shared memory)
 //   dV_j += P^T dO_i,  dK_j += dS^T Q_i (tcgen05, accumulators in TMEM)
 //   dQ_i  = dS K_j                      (tcgen05) -> fp32 reduce-adds into dq_accum
-// At the end dK_j * scale and dV_j are stored as bf16.  dQ = scale * dq_accum
-// is converted by a separate kernel.  The dQ and dK formulas follow from
-// S = scale Q K^T by the chain rule (the pages stop at dS).
+// At the end of an item dK_j * scale and dV_j are stored as bf16.  dQ = scale *
+// dq_accum is converted by a separate kernel.  The dQ and dK formulas follow
+// from S = scale Q K^T by the chain rule (the pages stop at dS).
+//
+// Persistent ("FlashAttention v1～v4" v4 §4 scheduling): one CTA per SM walks
+// items numbered heaviest first (causal: small j has the most Q tiles) and
+// dealt in snake order.  The Q/dO ring and every per-step barrier run on one
+// step counter across items, so the next item's first loads and MMAs start
+// while this item's last dQ tile drains and its dK/dV are written out: V is
+// released after the item's last dP^T, K after its last dQ, and dK/dV go from
+// TMEM straight to global memory (the K/V tiles are already being refilled).
 //
 // The global reduce-adds of dQ are capped per SM (about 25 bytes/cycle
 // measured on GB300, whatever the path), so a 64 KiB dQ tile costs ~2600
@@ -61,7 +69,7 @@ struct BwdCfg {
   static constexpr int kDsBytes = kTile * kTile * 2;
   static constexpr int kLdOff = kDsOff + kDsBytes;  // stage s: L2[128], D[128]
   static constexpr int kBarOff = kLdOff + 2 * 1024;
-  static constexpr int kNumBars = 17;
+  static constexpr int kNumBars = 21;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16;
   static constexpr uint32_t kColDK = kColDV + HD;
@@ -70,7 +78,7 @@ struct BwdCfg {
 
 // Barrier indices.
 enum : int {
-  kBarKv = 0,
+  kBarKFull = 0,   // K_j landed (phase = item parity)
   kBarQFull = 1,   // +stage: Q_i and the L / D vectors landed
   kBarQEmpty = 3,  // +stage: Q_i's half of the stage is free again
   kBarSFull = 5,
@@ -83,7 +91,31 @@ enum : int {
   kBarMmaDone = 12,
   kBarDoFull = 13,   // +stage: dO_i landed
   kBarDoEmpty = 15,  // +stage: dO_i's half of the stage is free again
+  kBarVFull = 17,    // V_j landed
+  kBarKEmpty = 18,   // the item's last MMA reading K_j has completed
+  kBarVEmpty = 19,   // the item's last MMA reading V_j has completed
+  kBarDkvEmpty = 20, // dK_j / dV_j have been read out of TMEM
 };
+
+// The m-th work item of this CTA: K/V tile j of head bh, with the Q tiles
+// i0 .. n_tiles-1.  Items are numbered heaviest first (k = j * BH + bh) and
+// dealt in snake order.  Returns false past the last item.
+struct BwdItem {
+  int j, bh, i0, n_it;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ bool get_bwd_item(int m, int n_tiles, int BH, BwdItem& w) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  const long long k = static_cast<long long>(m) * G + ((m & 1) ? (G - 1 - c) : c);
+  if (k >= static_cast<long long>(n_tiles) * BH) return false;
+  const int kk = static_cast<int>(k);
+  w.j = kk / BH;
+  w.bh = kk % BH;
+  w.i0 = CAUSAL ? w.j : 0;
+  w.n_it = n_tiles - w.i0;
+  return true;
+}
 
 template <int HD, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -108,14 +140,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int N = args.N;
   const int n_tiles = (N + kTile - 1) / kTile;
   const int pitch = n_tiles * kTile;
-  const int bh = blockIdx.x % args.BH;
-  const int j = blockIdx.x / args.BH;      // K/V tile; small j has the most Q tiles
-  const int kv0 = j * kTile;
-  const int i0 = CAUSAL ? j : 0;
-  const int n_it = n_tiles - i0;           // >= 1
+  const int BH = args.BH;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(kBarKv), 1);
+    mbar_init(bar(kBarKFull), 1);
+    mbar_init(bar(kBarVFull), 1);
+    mbar_init(bar(kBarKEmpty), 1);
+    mbar_init(bar(kBarVEmpty), 1);
+    mbar_init(bar(kBarDkvEmpty), kComputeThreads);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kBarQFull + s), 1);
       mbar_init(bar(kBarQEmpty + s), 1);
@@ -157,8 +189,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = warp >> 2;              // query columns [64*half, 64*half + 64)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;            // kv row of the tile = TMEM lane
-    const int kv = kv0 + r;
-    const bool kv_valid = kv < N;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tA = tmem + lane_off + kColA;
     const uint32_t tB = tmem + lane_off + kColB;
@@ -166,163 +196,179 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t ds_base = sbase + C::kDsOff;
     const int col0 = 64 * half;
     bool ok = true;
-    for (int it = 0; it < n_it && ok; ++it) {
-      const int i = i0 + it;
-      const int q0 = i * kTile;
-      const int s = it & 1;
-      const uint32_t ph = it & 1;
-      const uint32_t* nl2s =
-          reinterpret_cast<const uint32_t*>(smem + C::kLdOff + s * 1024) + col0;
-      const uint32_t* ds_vec = nl2s + 128;
-      // ---- P^T = 2^(S^T c - L2) (masked), this half's 64 query columns
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull), ph, wc, kWaitSFull));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t p0[32], p1[32];
-      tmem_ld32(tA + col0, p0);
-      tmem_ld32(tA + col0 + 32, p1);
-      tmem_ld_wait32(p0);
-      reg_fence32(p1);
-      uint32_t* pv[2] = {p0, p1};
-      const bool diag = CAUSAL && q0 == kv0;
-      // Only the diagonal tile and a K/V tile that runs past N need masks
-      // (warp-uniform test); padded query columns already get exponent -inf.
-      const bool need_mask = diag || kv0 + kTile > N;
-#pragma unroll
-      for (int g = 0; g < 2; ++g) {
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          // nl2 = -L*log2(e) per query column (-inf past N)
-          const uint4 l4 = *reinterpret_cast<const uint4*>(nl2s + g * 32 + e);
-          uint32_t x[4];
-          unpack2(ffma2(pack2(pv[g][e], pv[g][e + 1]), c2, pack2(l4.x, l4.y)), x[0], x[1]);
-          unpack2(ffma2(pack2(pv[g][e + 2], pv[g][e + 3]), c2, pack2(l4.z, l4.w)), x[2], x[3]);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) pv[g][e + u] = __float_as_uint(ex2_approx(__uint_as_float(x[u])));
-        }
-        if (need_mask) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int col = col0 + g * 32 + e;
-            if (!kv_valid || (diag && col < r)) pv[g][e] = 0u;
-          }
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(pv[g][2 * e]), __uint_as_float(pv[g][2 * e + 1]));
-        tmem_st16(tA + col0 + 16 * g, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(kBarPFull));
-      // ---- dS^T = P^T o (dP^T - D)
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDpFull), ph, wc, kWaitDpFull));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t dp0[32], dp1[32];
-      tmem_ld32(tB + col0, dp0);
-      tmem_ld32(tB + col0 + 32, dp1);
-      tmem_ld_wait32(dp0);
-      reg_fence32(dp1);
-      uint32_t* dpv[2] = {dp0, dp1};
-#pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const uint4 d4 = *reinterpret_cast<const uint4*>(ds_vec + g * 32 + e);
-          uint32_t y[4];
-          unpack2(fmul2(pack2(pv[g][e], pv[g][e + 1]),
-                        fsub2(pack2(dpv[g][e], dpv[g][e + 1]), pack2(d4.x, d4.y))),
-                  y[0], y[1]);
-          unpack2(fmul2(pack2(pv[g][e + 2], pv[g][e + 3]),
-                        fsub2(pack2(dpv[g][e + 2], dpv[g][e + 3]), pack2(d4.z, d4.w))),
-                  y[2], y[3]);
-          pk[e / 2] = pack_bf16x2(__uint_as_float(y[0]), __uint_as_float(y[1]));
-          pk[e / 2 + 1] = pack_bf16x2(__uint_as_float(y[2]), __uint_as_float(y[3]));
-        }
-        tmem_st16(tB + col0 + 16 * g, pk);
-        // dS row r, query columns [col0 + 32g, +32) = four 16-byte chunks of
-        // the MN-major (query-contiguous) operand: 64-column atoms, 128-byte
-        // swizzle inside each.
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          const int c16 = (col0 >> 3) + g * 4 + qq;
-          const uint32_t addr = ds_base + (c16 >> 3) * 16384 + r * 128 +
-                                (static_cast<uint32_t>((c16 & 7) ^ (r & 7)) << 4);
-          st_shared_v4(addr, pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
-        }
-      }
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(kBarDsFull));
-      // ---- dQ_i rows (TMEM lane = query row), this half's d/2 columns ->
-      // the Q/dO stage of this step (free now: every MMA that read it has
-      // completed), as 32 x 32 fp32 boxes with the 128-byte swizzle.
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDqFull), ph, wc, kWaitDqFull));
-      if (!ok) break;
-      tc_fence_after();
-      {
-        const uint32_t stage = sbase + C::kStageOff + s * C::kStageBytes;
-#pragma unroll
-        for (int ch = half * (HD / 64); ch < (half + 1) * (HD / 64); ++ch) {
-          uint32_t dq[32];
-          tmem_ld32(tB + 32 * ch, dq);
-          tmem_ld_wait32(dq);
-          const uint32_t box = stage + (wq * (HD / 32) + ch) * 4096;
-#pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4)
-            st_shared_v4(box + lane * 128 + (static_cast<uint32_t>(c4 ^ (lane & 7)) << 4),
-                         dq[4 * c4], dq[4 * c4 + 1], dq[4 * c4 + 2], dq[4 * c4 + 3]);
-        }
-        fence_proxy_async_smem();
-      }
-      tc_fence_before();
-      mbar_arrive(bar(kBarDqEmpty));
-    }
-    // ---- epilogue: warpgroup 0 stores dV_j, warpgroup 1 stores dK_j * scale
-    // (bf16, staged in the V / K tiles' shared memory, then TMA)
-    if (ok) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDkvFull), 0, wc, kWaitOFull));
-      if (ok) {
+    uint32_t step = 0;                       // steps done by this CTA (all items)
+    BwdItem w;
+    for (int m = 0; ok && get_bwd_item<CAUSAL>(m, n_tiles, BH, w); ++m) {
+      const int kv0 = w.j * kTile;
+      const int kv = kv0 + r;
+      const bool kv_valid = kv < N;
+      for (int it = 0; it < w.n_it; ++it, ++step) {
+        const int i = w.i0 + it;
+        const int q0 = i * kTile;
+        const int s = step & 1;
+        const uint32_t ph = step & 1;
+        const uint32_t* nl2s =
+            reinterpret_cast<const uint32_t*>(smem + C::kLdOff + s * 1024) + col0;
+        const uint32_t* ds_vec = nl2s + 128;
+        // ---- P^T = 2^(S^T c - L2) (masked), this half's 64 query columns
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull), ph, wc, kWaitSFull));
+        if (!ok) break;
         tc_fence_after();
-        const uint32_t tsrc = tmem + lane_off + (half == 0 ? kColDV : C::kColDK);
-        const float mul = half == 0 ? 1.f : args.scale;
-        const uint32_t stage = sbase + (half == 0 ? C::kVOff : C::kKOff);
-#pragma unroll 1
-        for (int ch = 0; ch < HD / 32; ++ch) {
-          uint32_t o[32];
-          tmem_ld32(tsrc + 32 * ch, o);
-          tmem_ld_wait32(o);
+        uint32_t p0[32], p1[32];
+        tmem_ld32(tA + col0, p0);
+        tmem_ld32(tA + col0 + 32, p1);
+        tmem_ld_wait32(p0);
+        reg_fence32(p1);
+        uint32_t* pv[2] = {p0, p1};
+        const bool diag = CAUSAL && q0 == kv0;
+        // Only the diagonal tile and a K/V tile that runs past N need masks
+        // (warp-uniform test); padded query columns already get exponent -inf.
+        const bool need_mask = diag || kv0 + kTile > N;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            // nl2 = -L*log2(e) per query column (-inf past N)
+            const uint4 l4 = *reinterpret_cast<const uint4*>(nl2s + g * 32 + e);
+            uint32_t x[4];
+            unpack2(ffma2(pack2(pv[g][e], pv[g][e + 1]), c2, pack2(l4.x, l4.y)), x[0], x[1]);
+            unpack2(ffma2(pack2(pv[g][e + 2], pv[g][e + 3]), c2, pack2(l4.z, l4.w)), x[2], x[3]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) pv[g][e + u] = __float_as_uint(ex2_approx(__uint_as_float(x[u])));
+          }
+          if (need_mask) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int col = col0 + g * 32 + e;
+              if (!kv_valid || (diag && col < r)) pv[g][e] = 0u;
+            }
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * mul,
-                                __uint_as_float(o[2 * e + 1]) * mul);
-          const uint32_t rowaddr = stage + (ch >> 1) * C::kChunkBytes + r * 128;
+            pk[e] = pack_bf16x2(__uint_as_float(pv[g][2 * e]), __uint_as_float(pv[g][2 * e + 1]));
+          tmem_st16(tA + col0 + 16 * g, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(kBarPFull));
+        // ---- dS^T = P^T o (dP^T - D)
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDpFull), ph, wc, kWaitDpFull));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t dp0[32], dp1[32];
+        tmem_ld32(tB + col0, dp0);
+        tmem_ld32(tB + col0 + 32, dp1);
+        tmem_ld_wait32(dp0);
+        reg_fence32(dp1);
+        uint32_t* dpv[2] = {dp0, dp1};
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const uint4 d4 = *reinterpret_cast<const uint4*>(ds_vec + g * 32 + e);
+            uint32_t y[4];
+            unpack2(fmul2(pack2(pv[g][e], pv[g][e + 1]),
+                          fsub2(pack2(dpv[g][e], dpv[g][e + 1]), pack2(d4.x, d4.y))),
+                    y[0], y[1]);
+            unpack2(fmul2(pack2(pv[g][e + 2], pv[g][e + 3]),
+                          fsub2(pack2(dpv[g][e + 2], dpv[g][e + 3]), pack2(d4.z, d4.w))),
+                    y[2], y[3]);
+            pk[e / 2] = pack_bf16x2(__uint_as_float(y[0]), __uint_as_float(y[1]));
+            pk[e / 2 + 1] = pack_bf16x2(__uint_as_float(y[2]), __uint_as_float(y[3]));
+          }
+          tmem_st16(tB + col0 + 16 * g, pk);
+          // dS row r, query columns [col0 + 32g, +32) = four 16-byte chunks of
+          // the MN-major (query-contiguous) operand: 64-column atoms, 128-byte
+          // swizzle inside each.
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq) {
-            const uint32_t chunk = (ch & 1) * 4 + qq;
-            st_shared_v4(rowaddr + ((chunk ^ (r & 7)) << 4), pk[4 * qq], pk[4 * qq + 1],
-                         pk[4 * qq + 2], pk[4 * qq + 3]);
+            const int c16 = (col0 >> 3) + g * 4 + qq;
+            const uint32_t addr = ds_base + (c16 >> 3) * 16384 + r * 128 +
+                                  (static_cast<uint32_t>((c16 & 7) ^ (r & 7)) << 4);
+            st_shared_v4(addr, pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
           }
         }
+        tmem_st_wait();
         fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && kv0 + wq * 32 < N) {
-          const CUtensorMap* tm = half == 0 ? &tm_dv : &tm_dk;
+        tc_fence_before();
+        mbar_arrive(bar(kBarDsFull));
+        // ---- dQ_i rows (TMEM lane = query row), this half's d/2 columns ->
+        // the Q/dO stage of this step (free now: every MMA that read it has
+        // completed), as 32 x 32 fp32 boxes with the 128-byte swizzle.
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDqFull), ph, wc, kWaitDqFull));
+        if (!ok) break;
+        tc_fence_after();
+        {
+          const uint32_t stage = sbase + C::kStageOff + s * C::kStageBytes;
 #pragma unroll
-          for (int cc = 0; cc < C::kChunks; ++cc)
-            tma_store_3d(tm, stage + cc * C::kChunkBytes + wq * 32 * 128, cc * 64, kv0 + wq * 32,
-                         bh);
-          bulk_commit_group();
-          bulk_wait_group_read0();
+          for (int ch = half * (HD / 64); ch < (half + 1) * (HD / 64); ++ch) {
+            uint32_t dq[32];
+            tmem_ld32(tB + 32 * ch, dq);
+            tmem_ld_wait32(dq);
+            const uint32_t box = stage + (wq * (HD / 32) + ch) * 4096;
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4)
+              st_shared_v4(box + lane * 128 + (static_cast<uint32_t>(c4 ^ (lane & 7)) << 4),
+                           dq[4 * c4], dq[4 * c4 + 1], dq[4 * c4 + 2], dq[4 * c4 + 3]);
+          }
+          fence_proxy_async_smem();
         }
+        tc_fence_before();
+        mbar_arrive(bar(kBarDqEmpty));
+      }
+      if (!ok) break;
+      // ---- item epilogue: warpgroup 0 writes dV_j, warpgroup 1 dK_j * scale,
+      // as bf16 64-column chunks staged with the 128-byte swizzle in this
+      // warpgroup's half of the dS buffer (free from the item's last dQ MMA
+      // until the next item's first dS) and stored by TMA, 32 rows per warp.
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDkvFull), m & 1, wc, kWaitOFull));
+      if (!ok) break;
+      tc_fence_after();
+      {
+        const uint32_t tsrc = tmem + lane_off + (half == 0 ? kColDV : C::kColDK);
+        const float mul = half == 0 ? 1.f : args.scale;
+        const uint32_t stage = ds_base + half * (kTile * 128);
+        const CUtensorMap* tm = half == 0 ? &tm_dv : &tm_dk;
+#pragma unroll 1
+        for (int cc = 0; cc < C::kChunks; ++cc) {
+          if (cc > 0) {
+            if (lane == 0) bulk_wait_group_read0();   // the previous chunk has been read
+            __syncwarp();
+          }
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t o[32];
+            tmem_ld32(tsrc + 32 * (2 * cc + hh), o);
+            tmem_ld_wait32(o);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * mul,
+                                  __uint_as_float(o[2 * e + 1]) * mul);
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              const uint32_t chunk = hh * 4 + qq;
+              st_shared_v4(stage + r * 128 + ((chunk ^ (r & 7)) << 4), pk[4 * qq],
+                           pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && kv0 + wq * 32 < N) {
+            tma_store_3d(tm, stage + wq * 32 * 128, cc * 64, kv0 + wq * 32, w.bh);
+            bulk_commit_group();
+          }
+        }
+        if (lane == 0) bulk_wait_group_read0();   // dS is written again next item
         __syncwarp();
       }
+      tc_fence_before();
+      mbar_arrive(bar(kBarDkvEmpty));
     }
+    if (lane == 0) bulk_wait_group0();   // the dK / dV stores have completed
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ================================================================ MMA issue
     // The whole warp runs this (converged); one elected lane issues.
@@ -352,56 +398,77 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts_w(d, tmem + a_col + (kk >> 2) * 64 + (kk & 3) * 8, db + ((kk * 2048) >> 4),
                    idesc_tm, kk > 0 ? 1u : acc);
       };
-      auto qfull = [&](int it) {
-        return mbar_wait_warp(bar(kBarQFull + (it & 1)), (it >> 1) & 1, wc, kWaitKvFull);
+      auto qfull = [&](uint32_t g) {
+        return mbar_wait_warp(bar(kBarQFull + (g & 1)), (g >> 1) & 1, wc, kWaitKvFull);
       };
-      auto dofull = [&](int it) {
-        return mbar_wait_warp(bar(kBarDoFull + (it & 1)), (it >> 1) & 1, wc, kWaitKvFull);
+      auto dofull = [&](uint32_t g) {
+        return mbar_wait_warp(bar(kBarDoFull + (g & 1)), (g >> 1) & 1, wc, kWaitKvFull);
       };
-      if (!mbar_wait_warp(bar(kBarKv), 0, wc, kWaitKvFull)) goto mma_end;
-      if (!qfull(0)) goto mma_end;
-      tc_fence_after();
-      mma_kmajor(tmem + kColA, sK, sQ(0));   // S^T
-      mma_commit_w(bar(kBarSFull));
-      if (!dofull(0)) goto mma_end;
-      tc_fence_after();
-      mma_kmajor(tmem + kColB, sV, sDo(0));  // dP^T
-      mma_commit_w(bar(kBarDpFull));
-      for (int it = 0; it < n_it; ++it) {
-        const int s = it & 1;
-        const uint32_t ph = it & 1;
-        const uint32_t acc = it > 0 ? 1u : 0u;
-        if (!mbar_wait_warp(bar(kBarPFull), ph, wc, kWaitPFull)) goto mma_end;
+      uint32_t step = 0;                     // steps issued by this CTA (all items)
+      BwdItem w;
+      for (int m = 0; get_bwd_item<CAUSAL>(m, n_tiles, BH, w); ++m) {
+        const int n_it = w.n_it;
+        const uint32_t s0 = step & 1;
+        // First S^T / dP^T of the item.  A is free (the previous item's last
+        // dV, which read P^T there, was issued before); B still holds the
+        // previous item's last dQ until the compute warps have parked it.
+        if (!mbar_wait_warp(bar(kBarKFull), m & 1, wc, kWaitKvFull)) goto mma_end;
+        if (!qfull(step)) goto mma_end;
         tc_fence_after();
-        mma_tmem_a(tmem + kColDV, kColA, sDo(s), acc);           // dV += P^T dO
-        if (!mbar_wait_warp(bar(kBarDsFull), ph, wc, kWaitDsFull)) goto mma_end;
+        mma_kmajor(tmem + kColA, sK, sQ(s0));   // S^T
+        mma_commit_w(bar(kBarSFull));
+        if (m > 0 && !mbar_wait_warp(bar(kBarDqEmpty), (step - 1) & 1, wc, kWaitDqEmpty))
+          goto mma_end;
+        if (!mbar_wait_warp(bar(kBarVFull), m & 1, wc, kWaitKvFull)) goto mma_end;
+        if (!dofull(step)) goto mma_end;
         tc_fence_after();
-        mma_tmem_a(tmem + C::kColDK, kColB, sQ(s), acc);         // dK += dS^T Q
-        // dQ = dS K into B (dS^T there has just been consumed by the dK MMA,
-        // issued before): A = dS (q contiguous, MN-major), B = K (HD contiguous).
-        {
-          const uint64_t dds = sdesc_sw128(sDs, 16384, 1024);
-          const uint64_t dk = sdesc_sw128(sK, C::kChunkBytes, 1024);
+        mma_kmajor(tmem + kColB, sV, sDo(s0));  // dP^T
+        mma_commit_w(bar(kBarDpFull));
+        if (n_it == 1) mma_commit_w(bar(kBarVEmpty));   // V_j's last reader issued
+        for (int it = 0; it < n_it; ++it, ++step) {
+          const int s = step & 1;
+          const uint32_t ph = step & 1;
+          const uint32_t acc = it > 0 ? 1u : 0u;
+          if (!mbar_wait_warp(bar(kBarPFull), ph, wc, kWaitPFull)) goto mma_end;
+          // The first dV / dK of an item overwrite the accumulators: the
+          // previous item's must have been read out.
+          if (it == 0 && m > 0 &&
+              !mbar_wait_warp(bar(kBarDkvEmpty), (m - 1) & 1, wc, kWaitOFull))
+            goto mma_end;
+          tc_fence_after();
+          mma_tmem_a(tmem + kColDV, kColA, sDo(s), acc);           // dV += P^T dO
+          if (!mbar_wait_warp(bar(kBarDsFull), ph, wc, kWaitDsFull)) goto mma_end;
+          tc_fence_after();
+          mma_tmem_a(tmem + C::kColDK, kColB, sQ(s), acc);         // dK += dS^T Q
+          // dQ = dS K into B (dS^T there has just been consumed by the dK MMA,
+          // issued before): A = dS (q contiguous, MN-major), B = K (HD contiguous).
+          {
+            const uint64_t dds = sdesc_sw128(sDs, 16384, 1024);
+            const uint64_t dk = sdesc_sw128(sK, C::kChunkBytes, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint32_t off = (kk * 2048) >> 4;
-            mma_ss_w(tmem + kColB, dds + off, dk + off, idesc_mm, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+              const uint32_t off = (kk * 2048) >> 4;
+              mma_ss_w(tmem + kColB, dds + off, dk + off, idesc_mm, kk > 0 ? 1u : 0u);
+            }
+          }
+          mma_commit_w(bar(kBarDqFull));
+          if (it + 1 < n_it) {
+            if (!qfull(step + 1)) goto mma_end;
+            tc_fence_after();
+            mma_kmajor(tmem + kColA, sK, sQ(s ^ 1));               // S^T (next), overlaps the dQ read-out
+            mma_commit_w(bar(kBarSFull));
+            if (!mbar_wait_warp(bar(kBarDqEmpty), ph, wc, kWaitDqEmpty)) goto mma_end;
+            if (!dofull(step + 1)) goto mma_end;
+            tc_fence_after();
+            mma_kmajor(tmem + kColB, sV, sDo(s ^ 1));              // dP^T (next)
+            mma_commit_w(bar(kBarDpFull));
+            if (it + 2 == n_it) mma_commit_w(bar(kBarVEmpty));   // V_j's last reader issued
+          } else {
+            mma_commit_w(bar(kBarKEmpty));     // K_j's last reader (this dQ) issued
+            mma_commit_w(bar(kBarDkvFull));    // dV_j / dK_j complete
           }
         }
-        mma_commit_w(bar(kBarDqFull));
-        if (it + 1 < n_it) {
-          if (!qfull(it + 1)) goto mma_end;
-          tc_fence_after();
-          mma_kmajor(tmem + kColA, sK, sQ(s ^ 1));               // S^T (next), overlaps the dQ read-out
-          mma_commit_w(bar(kBarSFull));
-          if (!mbar_wait_warp(bar(kBarDqEmpty), ph, wc, kWaitDqEmpty)) goto mma_end;
-          if (!dofull(it + 1)) goto mma_end;
-          tc_fence_after();
-          mma_kmajor(tmem + kColB, sV, sDo(s ^ 1));              // dP^T (next)
-          mma_commit_w(bar(kBarDpFull));
-        }
       }
-      mma_commit_w(bar(kBarDkvFull));
     mma_end:
       mma_commit_w(bar(kBarMmaDone));
       mbar_wait_drain(bar(kBarMmaDone), 0, args.wait_budget);
@@ -411,44 +478,77 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ TMA producer
     // Converged warp; one elected lane issues each copy.
     {
-      mbar_arrive_expect_tx_w(bar(kBarKv), 2 * C::kTileBytes);
-      for (int cc = 0; cc < C::kChunks; ++cc) {
-        tma_load_3d_w(sbase + C::kKOff + cc * C::kChunkBytes, &tm_k, bar(kBarKv), cc * 64, kv0,
-                      bh);
-        tma_load_3d_w(sbase + C::kVOff + cc * C::kChunkBytes, &tm_v, bar(kBarKv), cc * 64, kv0,
-                      bh);
-      }
       // Each stage is refilled in two halves, as the reduce warp frees them:
-      // Q_i with the L / D vectors (needed first, by S^T), then dO_i.
-      int issued_q = 0, issued_do = 0;
-      for (int it = 0; it < n_it; ++it) {
-        const int s = it & 1;
-        const int rnd = it >> 1;
-        const int q0 = (i0 + it) * kTile;
+      // Q_i with the L / D vectors (needed first, by S^T), then dO_i.  An
+      // item's V_j is loaded once the previous item's last dP^T has
+      // completed, its first Q_i / dO_i next, and K_j once the previous
+      // item's last dQ has completed; all four were prefetched into L2 while
+      // the previous item's last steps ran.
+      uint32_t step = 0;                     // Q and dO loads issued (steps)
+      uint32_t issued_q = 0, issued_do = 0;
+      int items_v = 0, items_k = 0;
+      BwdItem w;
+      bool ok = true;
+      // Q_i, the L / D vectors and dO_i of the CTA's next step into its stage.
+      auto load_step = [&](const BwdItem& wi, int it) -> bool {
+        const int s = step & 1;
+        const uint32_t rnd = step >> 1;
+        const int q0 = (wi.i0 + it) * kTile;
         const uint32_t dst = sbase + C::kStageOff + s * C::kStageBytes;
         if (rnd > 0 && !mbar_wait_warp(bar(kBarQEmpty + s), (rnd - 1) & 1, wc, kWaitKvEmpty))
-          break;
+          return false;
         const uint32_t qf = bar(kBarQFull + s);
         mbar_arrive_expect_tx_w(qf, C::kTileBytes + 1024);
         for (int cc = 0; cc < C::kChunks; ++cc)
-          tma_load_3d_w(dst + cc * C::kChunkBytes, &tm_q, qf, cc * 64, q0, bh);
-        const size_t vec = static_cast<size_t>(bh) * pitch + q0;
+          tma_load_3d_w(dst + cc * C::kChunkBytes, &tm_q, qf, cc * 64, q0, wi.bh);
+        const size_t vec = static_cast<size_t>(wi.bh) * pitch + q0;
         bulk_load_1d_w(sbase + C::kLdOff + s * 1024, args.L2 + vec, 512, qf);
         bulk_load_1d_w(sbase + C::kLdOff + s * 1024 + 512, args.D + vec, 512, qf);
-        issued_q = it + 1;
+        issued_q = step + 1;
         if (rnd > 0 && !mbar_wait_warp(bar(kBarDoEmpty + s), (rnd - 1) & 1, wc, kWaitKvEmpty))
-          break;
+          return false;
         const uint32_t df = bar(kBarDoFull + s);
         mbar_arrive_expect_tx_w(df, C::kTileBytes);
         for (int cc = 0; cc < C::kChunks; ++cc)
-          tma_load_3d_w(dst + C::kTileBytes + cc * C::kChunkBytes, &tm_do, df, cc * 64, q0, bh);
-        issued_do = it + 1;
+          tma_load_3d_w(dst + C::kTileBytes + cc * C::kChunkBytes, &tm_do, df, cc * 64, q0,
+                        wi.bh);
+        issued_do = step + 1;
+        ++step;
+        return true;
+      };
+      for (int m = 0; ok && get_bwd_item<CAUSAL>(m, n_tiles, BH, w); ++m) {
+        const int kv0 = w.j * kTile;
+        if (m > 0 && !mbar_wait_warp(bar(kBarVEmpty), (m - 1) & 1, wc, kWaitKvEmpty)) break;
+        mbar_arrive_expect_tx_w(bar(kBarVFull), C::kTileBytes);
+        for (int cc = 0; cc < C::kChunks; ++cc)
+          tma_load_3d_w(sbase + C::kVOff + cc * C::kChunkBytes, &tm_v, bar(kBarVFull), cc * 64,
+                        kv0, w.bh);
+        items_v = m + 1;
+        if (!load_step(w, 0)) break;
+        if (m > 0 && !mbar_wait_warp(bar(kBarKEmpty), (m - 1) & 1, wc, kWaitKvEmpty)) break;
+        mbar_arrive_expect_tx_w(bar(kBarKFull), C::kTileBytes);
+        for (int cc = 0; cc < C::kChunks; ++cc)
+          tma_load_3d_w(sbase + C::kKOff + cc * C::kChunkBytes, &tm_k, bar(kBarKFull), cc * 64,
+                        kv0, w.bh);
+        items_k = m + 1;
+        for (int it = 1; it < w.n_it && ok; ++it) ok = load_step(w, it);
+        BwdItem wn;
+        if (ok && get_bwd_item<CAUSAL>(m + 1, n_tiles, BH, wn)) {
+          for (int cc = 0; cc < C::kChunks; ++cc) {
+            tma_prefetch_l2_3d_w(&tm_k, cc * 64, wn.j * kTile, wn.bh);
+            tma_prefetch_l2_3d_w(&tm_v, cc * 64, wn.j * kTile, wn.bh);
+            tma_prefetch_l2_3d_w(&tm_q, cc * 64, wn.i0 * kTile, wn.bh);
+            tma_prefetch_l2_3d_w(&tm_do, cc * 64, wn.i0 * kTile, wn.bh);
+          }
+        }
       }
-      for (int it = max(0, issued_q - 2); it < issued_q; ++it)
-        mbar_wait_drain(bar(kBarQFull + (it & 1)), (it >> 1) & 1, args.wait_budget);
-      for (int it = max(0, issued_do - 2); it < issued_do; ++it)
-        mbar_wait_drain(bar(kBarDoFull + (it & 1)), (it >> 1) & 1, args.wait_budget);
-      mbar_wait_drain(bar(kBarKv), 0, args.wait_budget);
+      // Every copy this warp started must have landed before the CTA exits.
+      for (uint32_t g = issued_q > 2 ? issued_q - 2 : 0; g < issued_q; ++g)
+        mbar_wait_drain(bar(kBarQFull + (g & 1)), (g >> 1) & 1, args.wait_budget);
+      for (uint32_t g = issued_do > 2 ? issued_do - 2 : 0; g < issued_do; ++g)
+        mbar_wait_drain(bar(kBarDoFull + (g & 1)), (g >> 1) & 1, args.wait_budget);
+      if (items_v > 0) mbar_wait_drain(bar(kBarVFull), (items_v - 1) & 1, args.wait_budget);
+      if (items_k > 0) mbar_wait_drain(bar(kBarKFull), (items_k - 1) & 1, args.wait_budget);
     }
     __syncwarp();
   }
@@ -460,37 +560,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     // stage's Q half, rows 64-127 in its dO half -- and hand each half back
     // to the loader as soon as the TMA engine has read it.
     bool ok = true;
-    for (int it = 0; it < n_it && ok; ++it) {
-      const int s = it & 1;
-      const int q0 = (i0 + it) * kTile;
-      ok = mbar_wait_warp(bar(kBarDqEmpty), it & 1, wc, kWaitDqEmpty);
-      if (!ok) break;
-      if (lane == 0) {
-        // 8 KiB groups (two boxes), at most two in flight: the TMA engine
-        // serves the stage's loads in between instead of behind a whole
-        // 64 KiB reduce that drains at the per-SM reduce-add rate.
-        const uint32_t stage = sbase + C::kStageOff + s * C::kStageBytes;
-        for (int qb = 0; qb < 4; ++qb) {
+    uint32_t step = 0;
+    BwdItem w;
+    for (int m = 0; ok && get_bwd_item<CAUSAL>(m, n_tiles, BH, w); ++m) {
+      for (int it = 0; it < w.n_it; ++it, ++step) {
+        const int s = step & 1;
+        const int q0 = (w.i0 + it) * kTile;
+        const int bh = w.bh;
+        ok = mbar_wait_warp(bar(kBarDqEmpty), step & 1, wc, kWaitDqEmpty);
+        if (!ok) break;
+        if (lane == 0) {
+          // 8 KiB groups (two boxes), at most two in flight: the TMA engine
+          // serves the stage's loads in between instead of behind a whole
+          // 64 KiB reduce that drains at the per-SM reduce-add rate.
+          const uint32_t stage = sbase + C::kStageOff + s * C::kStageBytes;
+          for (int qb = 0; qb < 4; ++qb) {
 #pragma unroll
-          for (int ch = 0; ch < HD / 32; ch += 2) {
-            if (q0 + qb * 32 < N) {
-              tma_reduce_add_3d(&tm_dqacc, stage + (qb * (HD / 32) + ch) * 4096, ch * 32,
-                                q0 + qb * 32, bh);
-              tma_reduce_add_3d(&tm_dqacc, stage + (qb * (HD / 32) + ch + 1) * 4096,
-                                (ch + 1) * 32, q0 + qb * 32, bh);
+            for (int ch = 0; ch < HD / 32; ch += 2) {
+              if (q0 + qb * 32 < N) {
+                tma_reduce_add_3d(&tm_dqacc, stage + (qb * (HD / 32) + ch) * 4096, ch * 32,
+                                  q0 + qb * 32, bh);
+                tma_reduce_add_3d(&tm_dqacc, stage + (qb * (HD / 32) + ch + 1) * 4096,
+                                  (ch + 1) * 32, q0 + qb * 32, bh);
+              }
+              bulk_commit_group();
+              bulk_wait_group_read1();
             }
-            bulk_commit_group();
-            bulk_wait_group_read1();
+            if (qb == 1) {
+              bulk_wait_group_read0();
+              mbar_arrive(bar(kBarQEmpty + s));   // rows 0-63 (the Q half) read
+            }
           }
-          if (qb == 1) {
-            bulk_wait_group_read0();
-            mbar_arrive(bar(kBarQEmpty + s));   // rows 0-63 (the Q half) read
-          }
+          bulk_wait_group_read0();
+          mbar_arrive(bar(kBarDoEmpty + s));      // rows 64-127 (the dO half) read
         }
-        bulk_wait_group_read0();
-        mbar_arrive(bar(kBarDoEmpty + s));      // rows 64-127 (the dO half) read
+        __syncwarp();
       }
-      __syncwarp();
     }
     if (lane == 0) bulk_wait_group0();
     __syncwarp();
@@ -513,8 +618,13 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int n_tiles = (a.N + kTile - 1) / kTile;
-  const dim3 grid(static_cast<unsigned>(n_tiles * a.BH));
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  // Persistent grid: one CTA per SM (at most one per work item).
+  const long long items = static_cast<long long>((a.N + kTile - 1) / kTile) * a.BH;
+  const dim3 grid(static_cast<unsigned>(items < sms ? items : sms));
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdk, tdv, tacc, a);
   return cudaGetLastError();
 }

@@ -47,6 +47,7 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dO, const float* ls
 
 // tacc: 3-D fp32 view {d, N, B*H} of the dQ accumulator, 32 x 32 boxes,
 // 128-byte swizzle (the target of the dQ reduce-adds).
+// tdk, tdv: 64-column x 32-row boxes of dk, dv (the targets of the dK / dV stores).
 cudaError_t launch_bwd_main(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
                             const CUtensorMap& tdk, const CUtensorMap& tdv,

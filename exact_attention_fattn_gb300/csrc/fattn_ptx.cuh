@@ -306,6 +306,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_w(uint32_t bar, uint32_t b
       : "memory");
 }
 
+// Bring a tensor-map box into L2 (no shared-memory destination, no barrier);
+// one elected lane of a converged warp issues it.
+__device__ __forceinline__ void tma_prefetch_l2_3d_w(const void* tmap, int c0, int c1, int c2) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n\t}" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d_w(uint32_t dst, const void* tmap, uint32_t bar, int c0,
                                               int c1, int c2) {
   asm volatile(
