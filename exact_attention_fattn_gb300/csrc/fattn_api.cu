@@ -220,18 +220,18 @@ int bwd_main_impl(const void* q, const void* k, const void* v, const void* dO, v
   const BwdWorkspace ws = bwd_workspace(B, H, N, d);
   char* wbase = static_cast<char*>(workspace);
   int rc;
-  CUtensorMap tq, tk, tv, tdo, tdk, tdv, tacc;
+  CUtensorMap tq, tk, tv, tdo, tacc;
   if ((rc = make_map(&tq, q, N, BH, d, 128)) != FATTN_OK) return rc;
   if ((rc = make_map(&tk, k, N, BH, d, 128)) != FATTN_OK) return rc;
   if ((rc = make_map(&tv, v, N, BH, d, 128)) != FATTN_OK) return rc;
   if ((rc = make_map(&tdo, dO, N, BH, d, 128)) != FATTN_OK) return rc;
-  if ((rc = make_map(&tdk, dk, N, BH, d, 32)) != FATTN_OK) return rc;
-  if ((rc = make_map(&tdv, dv, N, BH, d, 32)) != FATTN_OK) return rc;
   if ((rc = make_acc_map(&tacc, wbase + ws.acc_off, N, BH, d)) != FATTN_OK) return rc;
   BwdArgs a;
   a.L2 = reinterpret_cast<const float*>(wbase + ws.l2_off);
   a.D = reinterpret_cast<const float*>(wbase + ws.d_off);
   a.dq_accum = reinterpret_cast<float*>(wbase + ws.acc_off);
+  a.dk = static_cast<uint16_t*>(dk);
+  a.dv = static_cast<uint16_t*>(dv);
   a.status = status;
   {
     std::lock_guard<std::mutex> lock(g_mu);
@@ -241,7 +241,7 @@ int bwd_main_impl(const void* q, const void* k, const void* v, const void* dO, v
   a.BH = BH;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
-  return from_cuda(launch_bwd_main(d, causal != 0, tq, tk, tv, tdo, tdk, tdv, tacc, a, st));
+  return from_cuda(launch_bwd_main(d, causal != 0, tq, tk, tv, tdo, tacc, a, st));
 }
 
 int bwd_finish_impl(const void* workspace, void* dq, int B, int H, int N, int d, float scale,

@@ -73,6 +73,11 @@ struct BwdCfg {
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16;
   static constexpr uint32_t kColDK = kColDV + HD;
+  // The two K/V tile slots swap roles every item (which = 0: K, 1: V), so the
+  // next item's K can land where this item's V was, one step before the end.
+  __device__ static constexpr int kv_off(int m, int which) {
+    return ((m ^ which) & 1) ? kVOff : kKOff;
+  }
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -121,7 +126,6 @@ template <int HD, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-               const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                const __grid_constant__ CUtensorMap tm_dqacc, const BwdArgs args) {
   using C = BwdCfg<HD>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -174,8 +178,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
-    tma_prefetch_desc(&tm_dk);
-    tma_prefetch_desc(&tm_dv);
     tma_prefetch_desc(&tm_dqacc);
   }
   tc_fence_before();
@@ -320,23 +322,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---- item epilogue: warpgroup 0 writes dV_j, warpgroup 1 dK_j * scale,
-      // as bf16 64-column chunks staged with the 128-byte swizzle in this
-      // warpgroup's half of the dS buffer (free from the item's last dQ MMA
-      // until the next item's first dS) and stored by TMA, 32 rows per warp.
+      // as bf16.  Each warp stages its 32 rows, one 64-column chunk at a
+      // time, in the part of the dS buffer that it writes dS into itself
+      // (free from the item's last dQ MMA until its next dS), and reads them
+      // back so that every store covers whole 128-byte row segments.
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDkvFull), m & 1, wc, kWaitOFull));
       if (!ok) break;
       tc_fence_after();
       {
         const uint32_t tsrc = tmem + lane_off + (half == 0 ? kColDV : C::kColDK);
         const float mul = half == 0 ? 1.f : args.scale;
-        const uint32_t stage = ds_base + half * (kTile * 128);
-        const CUtensorMap* tm = half == 0 ? &tm_dv : &tm_dk;
+        const uint32_t wbuf = ds_base + half * (kTile * 128) + wq * (32 * 128);
+        uint16_t* const out = (half == 0 ? args.dv : args.dk) + static_cast<size_t>(w.bh) * N * HD;
 #pragma unroll 1
         for (int cc = 0; cc < C::kChunks; ++cc) {
-          if (cc > 0) {
-            if (lane == 0) bulk_wait_group_read0();   // the previous chunk has been read
-            __syncwarp();
-          }
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             uint32_t o[32];
@@ -349,26 +348,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   __uint_as_float(o[2 * e + 1]) * mul);
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
-              const uint32_t chunk = hh * 4 + qq;
-              st_shared_v4(stage + r * 128 + ((chunk ^ (r & 7)) << 4), pk[4 * qq],
+              const uint32_t c16 = hh * 4 + qq;
+              st_shared_v4(wbuf + lane * 128 + ((c16 ^ (lane & 7)) << 4), pk[4 * qq],
                            pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
             }
           }
-          fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0 && kv0 + wq * 32 < N) {
-            tma_store_3d(tm, stage + wq * 32 * 128, cc * 64, kv0 + wq * 32, w.bh);
-            bulk_commit_group();
+          // 8 lanes per row, 4 rows per instruction.
+#pragma unroll
+          for (int rr = 0; rr < 32; rr += 4) {
+            const int lr = rr + (lane >> 3);
+            const uint32_t c16 = lane & 7;
+            const uint4 v = ld_shared_v4(wbuf + lr * 128 + ((c16 ^ (lr & 7)) << 4));
+            const int row = kv0 + wq * 32 + lr;
+            if (row < N)
+              *reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * HD + cc * 64 + c16 * 8) = v;
           }
+          __syncwarp();
         }
-        if (lane == 0) bulk_wait_group_read0();   // dS is written again next item
-        __syncwarp();
       }
       tc_fence_before();
       mbar_arrive(bar(kBarDkvEmpty));
     }
-    if (lane == 0) bulk_wait_group0();   // the dK / dV stores have completed
-    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ================================================================ MMA issue
     // The whole warp runs this (converged); one elected lane issues.
@@ -376,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_kk = idesc_bf16_f32(kTile, kTile, false, false);
       constexpr uint32_t idesc_tm = idesc_bf16_f32(kTile, HD, false, true);
       constexpr uint32_t idesc_mm = idesc_bf16_f32(kTile, HD, true, true);
-      const uint32_t sK = sbase + C::kKOff, sV = sbase + C::kVOff, sDs = sbase + C::kDsOff;
+      const uint32_t sDs = sbase + C::kDsOff;
       auto sQ = [&](int s) { return sbase + C::kStageOff + s * C::kStageBytes; };
       auto sDo = [&](int s) { return sbase + C::kStageOff + s * C::kStageBytes + C::kTileBytes; };
       // D(128 x 128) = A(128 x HD) B(128 x HD)^T, both K-major (HD contiguous).
@@ -409,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int m = 0; get_bwd_item<CAUSAL>(m, n_tiles, BH, w); ++m) {
         const int n_it = w.n_it;
         const uint32_t s0 = step & 1;
+        const uint32_t sK = sbase + C::kv_off(m, 0), sV = sbase + C::kv_off(m, 1);
         // First S^T / dP^T of the item.  A is free (the previous item's last
         // dV, which read P^T there, was issued before); B still holds the
         // previous item's last dQ until the compute warps have parked it.
@@ -480,10 +482,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       // Each stage is refilled in two halves, as the reduce warp frees them:
       // Q_i with the L / D vectors (needed first, by S^T), then dO_i.  An
-      // item's V_j is loaded once the previous item's last dP^T has
-      // completed, its first Q_i / dO_i next, and K_j once the previous
-      // item's last dQ has completed; all four were prefetched into L2 while
-      // the previous item's last steps ran.
+      // item's K_j is loaded once the previous item's last dP^T has
+      // completed (into that item's V slot), its first Q_i / dO_i next, and
+      // V_j once the previous item's last dQ has completed; all four were
+      // prefetched into L2 while the previous item's last steps ran.
       uint32_t step = 0;                     // Q and dO loads issued (steps)
       uint32_t issued_q = 0, issued_do = 0;
       int items_v = 0, items_k = 0;
@@ -518,19 +520,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int m = 0; ok && get_bwd_item<CAUSAL>(m, n_tiles, BH, w); ++m) {
         const int kv0 = w.j * kTile;
+        // K_j goes where the previous item's V was, V_j where its K was.
         if (m > 0 && !mbar_wait_warp(bar(kBarVEmpty), (m - 1) & 1, wc, kWaitKvEmpty)) break;
-        mbar_arrive_expect_tx_w(bar(kBarVFull), C::kTileBytes);
-        for (int cc = 0; cc < C::kChunks; ++cc)
-          tma_load_3d_w(sbase + C::kVOff + cc * C::kChunkBytes, &tm_v, bar(kBarVFull), cc * 64,
-                        kv0, w.bh);
-        items_v = m + 1;
-        if (!load_step(w, 0)) break;
-        if (m > 0 && !mbar_wait_warp(bar(kBarKEmpty), (m - 1) & 1, wc, kWaitKvEmpty)) break;
         mbar_arrive_expect_tx_w(bar(kBarKFull), C::kTileBytes);
         for (int cc = 0; cc < C::kChunks; ++cc)
-          tma_load_3d_w(sbase + C::kKOff + cc * C::kChunkBytes, &tm_k, bar(kBarKFull), cc * 64,
-                        kv0, w.bh);
+          tma_load_3d_w(sbase + C::kv_off(m, 0) + cc * C::kChunkBytes, &tm_k, bar(kBarKFull),
+                        cc * 64, kv0, w.bh);
         items_k = m + 1;
+        if (!load_step(w, 0)) break;
+        if (m > 0 && !mbar_wait_warp(bar(kBarKEmpty), (m - 1) & 1, wc, kWaitKvEmpty)) break;
+        mbar_arrive_expect_tx_w(bar(kBarVFull), C::kTileBytes);
+        for (int cc = 0; cc < C::kChunks; ++cc)
+          tma_load_3d_w(sbase + C::kv_off(m, 1) + cc * C::kChunkBytes, &tm_v, bar(kBarVFull),
+                        cc * 64, kv0, w.bh);
+        items_v = m + 1;
         for (int it = 1; it < w.n_it && ok; ++it) ok = load_step(w, it);
         BwdItem wn;
         if (ok && get_bwd_item<CAUSAL>(m + 1, n_tiles, BH, wn)) {
@@ -611,8 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int HD, bool CAUSAL>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                         const CUtensorMap& tacc, const BwdArgs& a, cudaStream_t stream) {
+                         const CUtensorMap& tdo, const CUtensorMap& tacc, const BwdArgs& a,
+                         cudaStream_t stream) {
   using C = BwdCfg<HD>;
   auto kern = bwd_kernel<HD, CAUSAL>;
   cudaError_t e =
@@ -625,7 +628,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   // Persistent grid: one CTA per SM (at most one per work item).
   const long long items = static_cast<long long>((a.N + kTile - 1) / kTile) * a.BH;
   const dim3 grid(static_cast<unsigned>(items < sms ? items : sms));
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdk, tdv, tacc, a);
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tacc, a);
   return cudaGetLastError();
 }
 
@@ -633,14 +636,13 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 cudaError_t launch_bwd_main(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
-                            const CUtensorMap& tdk, const CUtensorMap& tdv,
                             const CUtensorMap& tacc, const BwdArgs& a, cudaStream_t stream) {
   if (d == 64) {
-    return causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, tdk, tdv, tacc, a, stream)
-                  : launch_bwd_t<64, false>(tq, tk, tv, tdo, tdk, tdv, tacc, a, stream);
+    return causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, tacc, a, stream)
+                  : launch_bwd_t<64, false>(tq, tk, tv, tdo, tacc, a, stream);
   }
-  return causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, tdk, tdv, tacc, a, stream)
-                : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdk, tdv, tacc, a, stream);
+  return causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, tacc, a, stream)
+                : launch_bwd_t<128, false>(tq, tk, tv, tdo, tacc, a, stream);
 }
 
 }  // namespace fattn

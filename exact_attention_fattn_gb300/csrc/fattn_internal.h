@@ -31,6 +31,8 @@ struct BwdArgs {
   const float* L2;            // [BH, Np]: -lse * log2(e), -inf past N (Np = N rounded up to 128)
   const float* D;             // [BH, Np]: rowsum(dO o O), 0 past N
   float* dq_accum;            // [BH, N, d] fp32
+  uint16_t* dk;               // bf16 [BH, N, d]
+  uint16_t* dv;               // bf16 [BH, N, d]
   DeviceStatus* status;
   long long wait_budget;
   int N;
@@ -47,10 +49,8 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dO, const float* ls
 
 // tacc: 3-D fp32 view {d, N, B*H} of the dQ accumulator, 32 x 32 boxes,
 // 128-byte swizzle (the target of the dQ reduce-adds).
-// tdk, tdv: 64-column x 32-row boxes of dk, dv (the targets of the dK / dV stores).
 cudaError_t launch_bwd_main(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
-                            const CUtensorMap& tdk, const CUtensorMap& tdv,
                             const CUtensorMap& tacc, const BwdArgs& a, cudaStream_t stream);
 
 cudaError_t launch_dq_convert(const float* dq_accum, void* dq, long long elems, float scale,
