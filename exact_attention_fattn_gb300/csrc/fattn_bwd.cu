@@ -23,17 +23,19 @@
 //
 // The global reduce-adds of dQ are capped per SM (about 25 bytes/cycle
 // measured on GB300, whatever the path), so a 64 KiB dQ tile costs ~2600
-// cycles, as long as all five MMAs of the step.  They are therefore taken off
-// the critical path: the compute warps park the fp32 dQ tile in the Q/dO
-// shared-memory stage that the step has just finished with (64 KiB at d = 128,
-// 32 KiB at d = 64: exactly a dQ tile), in the 32 x 32 swizzled boxes of the
-// accumulator's tensor map, and go on; a reduce warp streams the boxes out
-// with TMA reduce-adds and only then hands the stage back to the loader.
+// cycles, longer than the step's five MMAs (~2560 cycles at the tensor
+// rate).  They are therefore taken off the critical path: a parking warpgroup
+// copies the fp32 dQ tile out of TMEM into the Q/dO shared-memory stage that
+// the step has just finished with (64 KiB at d = 128, 32 KiB at d = 64:
+// exactly a dQ tile), in the 32 x 32 swizzled boxes of the accumulator's
+// tensor map, which frees TMEM for the next dP^T; a reduce warp streams the
+// boxes out with TMA reduce-adds and only then hands the stage back to the
+// loader.  The compute warps never wait for either.
 //
 // Warps: 0-7 compute, as two warpgroups that split the 128 query columns of
 // every key row (P and dS are elementwise, so the halves never exchange
 // anything); 8 TMEM allocation + MMA issue; 9 TMA producer; 10 dQ reduce;
-// 11 idle.
+// 11 idle; 12-15 dQ parking.
 // TMEM (512 columns): A [0,128) holds S^T, then P^T; B [128,256) holds dP^T,
 // then dS^T, then dQ ([128,128+d)).  Each warpgroup packs its 64 bf16 values
 // (32 columns) into the first half of the 64 fp32 columns it read itself
@@ -49,11 +51,24 @@ namespace fattn {
 namespace {
 
 constexpr int kTile = 128;     // rows per Q tile and per K/V tile
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kComputeThreads = 256;
+constexpr int kParkThreads = 128;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kReduceWarp = 10;
+constexpr int kParkWarp0 = 12;
+// Register split: the kernel launches with kLaunchRegs per thread (512 x 128 =
+// 65,536); the compute warpgroups grow to kComputeRegs, the parking warpgroup
+// sets kParkRegs (two 32-column TMEM loads in flight) and the control
+// warpgroup (warps 8-11) shrinks to kCtrlRegs: 256 x 176 + 128 x 88 + 128 x 72
+// = 65,536, exactly the launch total, so setmaxnreg.inc can always complete.
+constexpr int kLaunchRegs = 128;
+constexpr int kComputeRegs = 176;
+constexpr int kParkRegs = 88;
+constexpr int kCtrlRegs = 72;
+static_assert(256 * kComputeRegs + 128 * kParkRegs + 128 * kCtrlRegs == kThreads * kLaunchRegs,
+              "register split");
 constexpr uint32_t kColA = 0, kColB = 128, kColDV = 256;
 
 template <int HD>
@@ -163,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarPFull), kComputeThreads);
     mbar_init(bar(kBarDsFull), kComputeThreads);
     mbar_init(bar(kBarDqFull), 1);
-    mbar_init(bar(kBarDqEmpty), kComputeThreads);
+    mbar_init(bar(kBarDqEmpty), kParkThreads);
     mbar_init(bar(kBarDkvFull), 1);
     mbar_init(bar(kBarMmaDone), 1);
     misc[1] = 0u;
@@ -187,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtx wc{args.wait_budget, reinterpret_cast<volatile uint32_t*>(&misc[1]), args.status};
 
   if (warp < 8) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kComputeRegs));
     // ================================================================ compute
     const int half = warp >> 2;              // query columns [64*half, 64*half + 64)
     const int wq = warp & 3;
@@ -296,29 +312,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(kBarDsFull));
-        // ---- dQ_i rows (TMEM lane = query row), this half's d/2 columns ->
-        // the Q/dO stage of this step (free now: every MMA that read it has
-        // completed), as 32 x 32 fp32 boxes with the 128-byte swizzle.
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDqFull), ph, wc, kWaitDqFull));
-        if (!ok) break;
-        tc_fence_after();
-        {
-          const uint32_t stage = sbase + C::kStageOff + s * C::kStageBytes;
-#pragma unroll
-          for (int ch = half * (HD / 64); ch < (half + 1) * (HD / 64); ++ch) {
-            uint32_t dq[32];
-            tmem_ld32(tB + 32 * ch, dq);
-            tmem_ld_wait32(dq);
-            const uint32_t box = stage + (wq * (HD / 32) + ch) * 4096;
-#pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4)
-              st_shared_v4(box + lane * 128 + (static_cast<uint32_t>(c4 ^ (lane & 7)) << 4),
-                           dq[4 * c4], dq[4 * c4 + 1], dq[4 * c4 + 2], dq[4 * c4 + 3]);
-          }
-          fence_proxy_async_smem();
-        }
-        tc_fence_before();
-        mbar_arrive(bar(kBarDqEmpty));
       }
       if (!ok) break;
       // ---- item epilogue: warpgroup 0 writes dV_j, warpgroup 1 dK_j * scale,
@@ -371,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(kBarDkvEmpty));
     }
   } else if (warp == kMmaWarp) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
     // ================================================================ MMA issue
     // The whole warp runs this (converged); one elected lane issues.
     {
@@ -477,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == kLoadWarp) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
     // ================================================================ TMA producer
     // Converged warp; one elected lane issues each copy.
     {
@@ -554,9 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (items_k > 0) mbar_wait_drain(bar(kBarKFull), (items_k - 1) & 1, args.wait_budget);
     }
     __syncwarp();
-  }
-
-  if (warp == kReduceWarp) {
+  } else if (warp == kReduceWarp) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
     // ================================================================ dQ reduce
     // For each step: once the compute warps have parked dQ_i in stage s,
     // reduce-add its boxes into the accumulator -- query rows 0-63 sit in the
@@ -602,6 +596,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) bulk_wait_group0();
     __syncwarp();
+  } else if (warp >= kParkWarp0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kParkRegs));
+    // ================================================================ dQ parking
+    // For each step: dQ_i rows (TMEM lane = query row), all d columns -> the
+    // Q/dO stage of the step (free now: every MMA that read it has
+    // completed), as 32 x 32 fp32 boxes with the 128-byte swizzle.  Query
+    // rows 0-63 land in the stage's Q half, 64-127 in its dO half.
+    const int wq = warp & 3;
+    const uint32_t tB = tmem + (static_cast<uint32_t>(wq * 32) << 16) + kColB;
+    bool ok = true;
+    uint32_t step = 0;
+    BwdItem w;
+    for (int m = 0; ok && get_bwd_item<CAUSAL>(m, n_tiles, BH, w); ++m) {
+      for (int it = 0; it < w.n_it; ++it, ++step) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDqFull), step & 1, wc, kWaitDqFull));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t stage = sbase + C::kStageOff + (step & 1) * C::kStageBytes;
+#pragma unroll
+        for (int ch = 0; ch < HD / 32; ch += 2) {
+          uint32_t d0[32], d1[32];
+          tmem_ld32(tB + 32 * ch, d0);
+          tmem_ld32(tB + 32 * (ch + 1), d1);
+          tmem_ld_wait32(d0);
+          reg_fence32(d1);
+          const uint32_t box0 = stage + (wq * (HD / 32) + ch) * 4096 + lane * 128;
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const uint32_t sw = static_cast<uint32_t>(c4 ^ (lane & 7)) << 4;
+            st_shared_v4(box0 + sw, d0[4 * c4], d0[4 * c4 + 1], d0[4 * c4 + 2], d0[4 * c4 + 3]);
+            st_shared_v4(box0 + 4096 + sw, d1[4 * c4], d1[4 * c4 + 1], d1[4 * c4 + 2],
+                         d1[4 * c4 + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(kBarDqEmpty));
+      }
+    }
+  } else {
+    // warp 11: no work; it only hands its registers back.
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
   }
 
   tc_fence_before();
@@ -621,6 +657,11 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
+  // The register split inside the kernel is only valid for this launch size.
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
