@@ -16,6 +16,7 @@ from .attention import (  # noqa: F401
     fattn_check_status,
     fattn_fwd,
     fattn_selftest_timeout,
+    fattn_set_deterministic,
     fattn_set_rescale_threshold,
     fattn_set_wait_budget,
     workspace_for,

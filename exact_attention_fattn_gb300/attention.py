@@ -149,6 +149,11 @@ def fattn_set_rescale_threshold(tau_log2: float) -> None:
     _lib.load().fattn_set_rescale_threshold(float(tau_log2))
 
 
+def fattn_set_deterministic(on: bool) -> None:
+    """dQ accumulated in a fixed order (bitwise reproducible backward)."""
+    _lib.load().fattn_set_deterministic(1 if on else 0)
+
+
 def fattn_selftest_timeout(budget_cycles: int, device=None) -> int:
     dev = torch.device("cuda") if device is None else torch.device(device)
     lib = _lib.load()

@@ -25,6 +25,7 @@ DeviceStatus* g_status_ptr[kMaxDevices] = {};
 int g_arch_ok[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 unsupported
 long long g_budget = kDefaultBudget;
 float g_tau_log2 = 8.0f;
+bool g_deterministic = false;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -152,11 +153,12 @@ int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, 
 
 // Workspace of the backward pass: D and -L*log2(e) in a [B*H, Np] layout
 // (Np = N rounded up to the 128-row tile, so that every tile's 512-byte
-// slice can be fetched by one bulk copy), then the fp32 dQ accumulator.
+// slice can be fetched by one bulk copy), then the fp32 dQ accumulator, then
+// one uint32 dQ contribution counter per (head, 128-row Q tile).
 }  // extern "C"
 namespace {
 struct BwdWorkspace {
-  size_t d_off, l2_off, acc_off, total;
+  size_t d_off, l2_off, acc_off, cnt_off, total;
   int pitch;
 };
 
@@ -168,7 +170,8 @@ BwdWorkspace bwd_workspace(int B, int H, int N, int d) {
   w.d_off = 0;
   w.l2_off = align256(prow * sizeof(float));
   w.acc_off = w.l2_off + align256(prow * sizeof(float));
-  w.total = w.acc_off + align256(rows * d * sizeof(float));
+  w.cnt_off = w.acc_off + align256(rows * d * sizeof(float));
+  w.total = w.cnt_off + align256(static_cast<size_t>(B) * H * (w.pitch / 128) * sizeof(uint32_t));
   return w;
 }
 }  // namespace
@@ -188,8 +191,8 @@ int fattn_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_accu
     return FATTN_ERR_INVALID_ARG;
   DeviceStatus* status = nullptr;
   if ((rc = device_setup(&status)) != FATTN_OK) return rc;
-  return from_cuda(launch_bwd_preprocess(o, dO, nullptr, D, nullptr, dq_accum, B * H, N, N, d,
-                                         reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_bwd_preprocess(o, dO, nullptr, D, nullptr, dq_accum, nullptr, B * H,
+                                         N, N, d, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"
@@ -210,7 +213,7 @@ int bwd_prepare_impl(const void* o, const void* dO, const float* lse, void* work
   return from_cuda(launch_bwd_preprocess(
       o, dO, lse, reinterpret_cast<float*>(wbase + ws.d_off),
       reinterpret_cast<float*>(wbase + ws.l2_off), reinterpret_cast<float*>(wbase + ws.acc_off),
-      B * H, N, ws.pitch, d, st));
+      reinterpret_cast<uint32_t*>(wbase + ws.cnt_off), B * H, N, ws.pitch, d, st));
 }
 
 int bwd_main_impl(const void* q, const void* k, const void* v, const void* dO, void* workspace,
@@ -236,6 +239,7 @@ int bwd_main_impl(const void* q, const void* k, const void* v, const void* dO, v
   {
     std::lock_guard<std::mutex> lock(g_mu);
     a.wait_budget = g_budget;
+    a.dq_order = g_deterministic ? reinterpret_cast<uint32_t*>(wbase + ws.cnt_off) : nullptr;
   }
   a.N = N;
   a.BH = BH;
@@ -355,6 +359,11 @@ const char* fattn_status_string(int status) {
 void fattn_set_wait_budget(long long cycles) {
   std::lock_guard<std::mutex> lock(g_mu);
   g_budget = cycles > 0 ? cycles : kDefaultBudget;
+}
+
+void fattn_set_deterministic(int on) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_deterministic = on != 0;
 }
 
 void fattn_set_rescale_threshold(float tau_log2) {

@@ -552,10 +552,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kReduceWarp) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
     // ================================================================ dQ reduce
-    // For each step: once the compute warps have parked dQ_i in stage s,
-    // reduce-add its boxes into the accumulator -- query rows 0-63 sit in the
-    // stage's Q half, rows 64-127 in its dO half -- and hand each half back
-    // to the loader as soon as the TMA engine has read it.
+    // For each step: once dQ_i has been parked in stage s, reduce-add its
+    // boxes into the accumulator -- query rows 0-63 sit in the stage's Q
+    // half, rows 64-127 in its dO half -- and hand each half back to the
+    // loader as soon as the TMA engine has read it.  In deterministic mode
+    // ("FlashAttention v1～v4" v4 §4) the adds into Q tile i wait for the
+    // tile's counter to show that K/V tiles 0..j-1 have added theirs, and the
+    // counter moves on to j+1 once this tile's adds have completed.
+    uint32_t* const order = args.dq_order;
     bool ok = true;
     uint32_t step = 0;
     BwdItem w;
@@ -566,6 +570,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int bh = w.bh;
         ok = mbar_wait_warp(bar(kBarDqEmpty), step & 1, wc, kWaitDqEmpty);
         if (!ok) break;
+        uint32_t* const cnt =
+            order != nullptr ? order + static_cast<size_t>(bh) * n_tiles + (w.i0 + it) : nullptr;
+        if (cnt != nullptr) {
+          bool turn = true;
+          if (lane == 0) {
+            turn = counter_wait(cnt, static_cast<uint32_t>(w.j), wc, kWaitDqOrder);
+            fence_proxy_async_global();
+          }
+          ok = __shfl_sync(0xffffffffu, turn ? 1 : 0, 0) != 0;
+          if (!ok) break;
+        }
         if (lane == 0) {
           // 8 KiB groups (two boxes), at most two in flight: the TMA engine
           // serves the stage's loads in between instead of behind a whole
@@ -590,6 +605,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           bulk_wait_group_read0();
           mbar_arrive(bar(kBarDoEmpty + s));      // rows 64-127 (the dO half) read
+          if (cnt != nullptr) {
+            bulk_wait_group0();                   // the adds themselves have completed
+            fence_proxy_async_global();
+            st_release_gpu(cnt, static_cast<uint32_t>(w.j) + 1u);
+          }
         }
         __syncwarp();
       }

@@ -2,7 +2,7 @@
 //
 //  preprocess: D_i = sum_k dO_ik O_ik ("6.1 FlashAttention V1详解" §6.1,
 //              the identity rowsum(dP o P) = rowsum(dO o O)), and zero the
-//              fp32 dQ accumulator.
+//              fp32 dQ accumulator and the dQ contribution counters.
 //  dq convert: dq = bf16(scale * dq_accum) (the scale of dQ = scale dS K is
 //              applied once here instead of on every partial sum).
 #include "fattn_internal.h"
@@ -34,12 +34,14 @@ __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b) {
 //   D[bh*pitch + n]  = sum_k dO O,
 //   L2[bh*pitch + n] = -lse[bh*N + n] * log2(e)      (when L2 is given),
 // and the padding rows n >= N get D = 0 and L2 = -inf (a column that no
-// probability can reach: 2^(s*scale*log2e - inf) = 0).
+// probability can reach: 2^(s*scale*log2e - inf) = 0).  The first row of
+// every 128-row tile also zeroes that tile's counter (pitch is a multiple of
+// 128 whenever counters are given).
 template <int HD>
 __global__ void __launch_bounds__(kAuxThreads) preprocess_kernel(
     const uint4* __restrict__ o, const uint4* __restrict__ dO, const float* __restrict__ lse,
-    float* __restrict__ D, float* __restrict__ L2, float4* __restrict__ dq_accum, int N,
-    int pitch, long long padded_rows) {
+    float* __restrict__ D, float* __restrict__ L2, float4* __restrict__ dq_accum,
+    uint32_t* __restrict__ counters, int N, int pitch, long long padded_rows) {
   constexpr int kTpr = HD / 8;          // threads per row
   constexpr int kRowsPerWarp = 32 / kTpr;
   const int lane = threadIdx.x & 31;
@@ -61,6 +63,7 @@ __global__ void __launch_bounds__(kAuxThreads) preprocess_kernel(
 #pragma unroll
     for (int off = kTpr / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (in_range && sub == 0) {
+      if (counters != nullptr && (n & 127) == 0) counters[bh * (pitch >> 7) + (n >> 7)] = 0u;
       D[prow] = s;
       if (L2 != nullptr) L2[prow] = valid ? -__ldg(&lse[row]) * 1.4426950408889634f : -INFINITY;
     }
@@ -115,18 +118,18 @@ int grid_for(long long work_items) {
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, const float* lse, float* D,
-                                  float* L2, float* dq_accum, int BH, int N, int pitch, int d,
-                                  cudaStream_t stream) {
+                                  float* L2, float* dq_accum, uint32_t* counters, int BH, int N,
+                                  int pitch, int d, cudaStream_t stream) {
   const long long padded_rows = static_cast<long long>(BH) * pitch;
   const int grid = grid_for(padded_rows * (d / 8));
   if (d == 64) {
     preprocess_kernel<64><<<grid, kAuxThreads, 0, stream>>>(
         static_cast<const uint4*>(o), static_cast<const uint4*>(dO), lse, D, L2,
-        reinterpret_cast<float4*>(dq_accum), N, pitch, padded_rows);
+        reinterpret_cast<float4*>(dq_accum), counters, N, pitch, padded_rows);
   } else {
     preprocess_kernel<128><<<grid, kAuxThreads, 0, stream>>>(
         static_cast<const uint4*>(o), static_cast<const uint4*>(dO), lse, D, L2,
-        reinterpret_cast<float4*>(dq_accum), N, pitch, padded_rows);
+        reinterpret_cast<float4*>(dq_accum), counters, N, pitch, padded_rows);
   }
   return cudaGetLastError();
 }

@@ -31,6 +31,7 @@ struct BwdArgs {
   const float* L2;            // [BH, Np]: -lse * log2(e), -inf past N (Np = N rounded up to 128)
   const float* D;             // [BH, Np]: rowsum(dO o O), 0 past N
   float* dq_accum;            // [BH, N, d] fp32
+  uint32_t* dq_order;         // [BH, n_tiles] contribution counters, or nullptr (any order)
   uint16_t* dk;               // bf16 [BH, N, d]
   uint16_t* dv;               // bf16 [BH, N, d]
   DeviceStatus* status;
@@ -42,10 +43,11 @@ struct BwdArgs {
 };
 
 // D (and, when L2 != nullptr, L2 = -lse * log2 e) in a [BH, pitch] layout with
-// padding rows N..pitch-1; zeroes dq_accum [BH, N, d].
+// padding rows N..pitch-1; zeroes dq_accum [BH, N, d] and, when given, the
+// [BH, pitch / 128] dQ contribution counters.
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, const float* lse, float* D,
-                                  float* L2, float* dq_accum, int BH, int N, int pitch, int d,
-                                  cudaStream_t stream);
+                                  float* L2, float* dq_accum, uint32_t* counters, int BH, int N,
+                                  int pitch, int d, cudaStream_t stream);
 
 // tacc: 3-D fp32 view {d, N, B*H} of the dQ accumulator, 32 x 32 boxes,
 // 128-byte swizzle (the target of the dQ reduce-adds).

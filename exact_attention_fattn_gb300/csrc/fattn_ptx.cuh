@@ -32,6 +32,7 @@ enum WaitSite : unsigned int {
   kWaitDqFull = 11,
   kWaitDqEmpty = 12,
   kWaitDpFull = 13,
+  kWaitDqOrder = 14,
 };
 
 constexpr unsigned int kStatusTimeout = 4;  // == FATTN_ERR_TIMEOUT
@@ -186,6 +187,41 @@ __device__ __forceinline__ void red_add_f32(float* gaddr, uint32_t v) {
 // Make generic-proxy shared-memory writes visible to the async proxy (TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's generic-proxy accesses to global memory with its
+// async-proxy ones (TMA copies and reduce-adds).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ counters
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait until the global counter *c reaches `target` (another CTA's release);
+// bounded like mbar_wait.
+__device__ __forceinline__ bool counter_wait(const uint32_t* c, uint32_t target, const WaitCtx& w,
+                                             unsigned int site) {
+  if (ld_acquire_gpu(c) >= target) return true;
+  const long long t0 = clock64();
+  while (true) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(c) >= target) return true;
+    if (*w.abort) return false;
+    if (clock64() - t0 > w.budget) {
+      record_timeout(w, site);
+      return false;
+    }
+  }
 }
 
 // ------------------------------------------------------------------ tcgen05

@@ -77,8 +77,9 @@ int fattn_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_accu
 /*
  * Workspace the backward pass needs, in bytes: D and -L*log2(e) (fp32, each
  * [B*H, Np] with Np = N rounded up to a multiple of 128), then the fp32 dQ
- * accumulator ([B,H,N,d]); each part starts on a 256-byte boundary.
- * Returns 0 for invalid sizes.
+ * accumulator ([B,H,N,d]), then one uint32 dQ contribution counter per head
+ * and 128-row Q tile ([B*H, Np/128], used in deterministic mode); each part
+ * starts on a 256-byte boundary.  Returns 0 for invalid sizes.
  */
 size_t fattn_bwd_workspace_bytes(int B, int H, int N, int d);
 
@@ -92,7 +93,8 @@ size_t fattn_bwd_workspace_bytes(int B, int H, int N, int d);
  *   workspace      : scratch of at least fattn_bwd_workspace_bytes(B,H,N,d),
  *                    256-byte aligned, caller-owned; contents on entry ignored
  * Enqueues, in order: preprocess, the main backward kernel (dQ accumulated
- * with fp32 atomics), and the dQ conversion.  Returns a fattn_status.
+ * with fp32 reduce-adds, in a fixed order when fattn_set_deterministic is on),
+ * and the dQ conversion.  Returns a fattn_status.
  */
 int fattn_bwd(const void* q, const void* k, const void* v, const void* o,
               const void* dO, const float* lse, void* dq, void* dk, void* dv,
@@ -175,6 +177,21 @@ const char* fattn_status_string(int status);
  * Applies to launches made after the call, from any thread.
  */
 void fattn_set_wait_budget(long long cycles);
+
+/*
+ * Deterministic backward ("FlashAttention v1～v4" v4 §4: cross-CTA
+ * reductions in a fixed order through semaphores).  When on, every 128-row
+ * tile of the fp32 dQ accumulator receives the contributions of the K/V tiles
+ * in ascending tile order: the CTA holding K/V tile j waits (bounded by the
+ * wait budget; a wait that runs out is a FATTN_ERR_TIMEOUT) until the
+ * workspace counter of the Q tile says that tiles 0..j-1 have been added,
+ * adds its own, waits for its adds to complete and advances the counter.
+ * dQ, dK and dV are then bitwise identical from run to run for the same
+ * inputs and device (dK and dV always are).  Off by default: dQ is otherwise
+ * summed in arrival order, which differs run to run within fp32 rounding.
+ * Applies to backward launches made after the call, from any thread.
+ */
+void fattn_set_deterministic(int on);
 
 /*
  * Threshold, in log2 units, of the conditional rescaling in the forward pass

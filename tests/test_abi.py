@@ -56,7 +56,9 @@ def test_workspace_bytes(lib):
     for B, H, N, d in ((1, 1, 1, 64), (2, 32, 4096, 128), (1, 16, 16384, 128), (3, 5, 77, 64)):
         rows = B * H * N
         np_ = (N + 127) // 128 * 128
-        assert lib.fattn_bwd_workspace_bytes(B, H, N, d) == 2 * al(4 * B * H * np_) + al(4 * rows * d)
+        counters = al(4 * B * H * (np_ // 128))
+        assert lib.fattn_bwd_workspace_bytes(B, H, N, d) == (2 * al(4 * B * H * np_)
+                                                             + al(4 * rows * d) + counters)
     assert lib.fattn_bwd_workspace_bytes(0, 1, 1, 64) == 0
     assert lib.fattn_bwd_workspace_bytes(1, 1, 1, 96) == 0
 
