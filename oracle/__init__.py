@@ -29,3 +29,11 @@ from .attention import (  # noqa: F401
     flash_forward_kv_outer_v1,
     flash_forward_q_outer,
 )
+from .fp8 import (  # noqa: F401
+    E4M3_MAX,
+    e4m3_decode,
+    e4m3_encode,
+    block_quantize,
+    block_dequantize,
+    attention_fp8_reference,
+)
