@@ -15,6 +15,8 @@ from .attention import (  # noqa: F401
     fattn_bwd_workspace_bytes,
     fattn_check_status,
     fattn_fwd,
+    fattn_fwd_fp8,
+    fattn_quantize_fp8,
     fattn_selftest_timeout,
     fattn_set_deterministic,
     fattn_set_rescale_threshold,

@@ -26,6 +26,10 @@ _c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, 
 SIGNATURES = {
     "fattn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                            _c_float, _vp]),
+    "fattn_fp8_codes_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "fattn_quantize_fp8": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
+    "fattn_fwd_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
+                               _c_int, _c_int, _c_float, _vp]),
     "fattn_bwd_preprocess": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp]),
     "fattn_bwd_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "fattn_bwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_size,

@@ -53,6 +53,54 @@ def fattn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=Non
     return o, l
 
 
+def fattn_quantize_fp8(x, transposed: bool = False):
+    """Block-quantize a bf16 [B,H,N,d] tensor (d = 128) to e4m3 codes.
+
+    Returns (codes, scales): uint8 [B,H,N,d] (or [B,H,d,Np] when
+    ``transposed``, Np = N rounded up to 128) and fp32 [B,H,ceil(N/128)].
+    """
+    _check_inputs([x])
+    B, H, N, d = x.shape
+    lib = _lib.load()
+    nbytes = int(lib.fattn_fp8_codes_bytes(B, H, N, d, int(bool(transposed))))
+    if nbytes == 0:
+        raise ValueError("the FP8 path supports d = 128 only")
+    np_ = (N + 127) // 128 * 128
+    shape = (B, H, d, np_) if transposed else (B, H, N, d)
+    codes = torch.empty(shape, dtype=torch.uint8, device=x.device)
+    scales = torch.empty((B, H, (N + 127) // 128), dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        rc = lib.fattn_quantize_fp8(x.data_ptr(), codes.data_ptr(), scales.data_ptr(), B, H, N, d,
+                                    int(bool(transposed)), _stream_ptr(x.device))
+    _lib.check("fattn_quantize_fp8", rc)
+    return codes, scales
+
+
+def fattn_fwd_fp8(q8, sq, k8, sk, v8t, sv, causal: bool = False, scale: float | None = None,
+                  out=None, lse=None):
+    """FP8 forward on block-quantized inputs (from fattn_quantize_fp8; V
+    transposed); returns (O bf16 [B,H,N,d], L fp32 [B,H,N])."""
+    for t in (q8, k8, v8t):
+        if t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError("q8, k8, v8t must be contiguous uint8 CUDA tensors")
+    for t in (sq, sk, sv):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise TypeError("scales must be contiguous fp32 tensors")
+    B, H, N, d = q8.shape
+    if k8.shape != q8.shape or v8t.shape[:3] != (B, H, d):
+        raise ValueError("q8, k8 must be [B,H,N,d] and v8t [B,H,d,Np]")
+    scale = default_scale(d) if scale is None else float(scale)
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    lib = _lib.load()
+    with torch.cuda.device(q8.device):
+        rc = lib.fattn_fwd_fp8(q8.data_ptr(), sq.data_ptr(), k8.data_ptr(), sk.data_ptr(),
+                               v8t.data_ptr(), sv.data_ptr(), o.data_ptr(), l.data_ptr(),
+                               B, H, N, d, int(bool(causal)), scale, _stream_ptr(q8.device))
+    _lib.check("fattn_fwd_fp8", rc)
+    return o, l
+
+
 def fattn_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return int(_lib.load().fattn_bwd_workspace_bytes(B, H, N, d))
 

@@ -93,6 +93,22 @@ int make_map(CUtensorMap* m, const void* ptr, int N, int BH, int d, int box_rows
   return r == CUDA_SUCCESS ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
+// 3-D uint8 view {inner, rows, B*H} of e4m3 codes, 128-byte x 128-row boxes,
+// 128-byte swizzle, zero fill outside the tensor.
+int make_map_u8(CUtensorMap* m, const void* ptr, int inner, int rows, int BH) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner),
+                                 static_cast<cuuint64_t>(rows) * inner};
+  const cuuint32_t box[3] = {128u, 128u, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
 // 3-D fp32 view {d, N, B*H} of the dQ accumulator: 32-column (128-byte) x
 // 32-row boxes, 128-byte swizzle.
 int make_acc_map(CUtensorMap* m, const void* ptr, int N, int BH, int d) {
@@ -142,6 +158,7 @@ int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, 
   a.N = N;
   a.BH = BH;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.sq = a.sk = a.sv = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     a.wait_budget = g_budget;
@@ -149,6 +166,65 @@ int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, 
   }
   return from_cuda(launch_fwd(d, causal != 0, tq, tk, tv, a,
                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t fattn_fp8_codes_bytes(int B, int H, int N, int d, int transposed) {
+  if (check_sizes(B, H, N, d) != FATTN_OK || d != 128) return 0;
+  const size_t rows = transposed ? static_cast<size_t>(N + 127) / 128 * 128 : N;
+  return static_cast<size_t>(B) * H * rows * d;
+}
+
+int fattn_quantize_fp8(const void* x, void* codes, float* scales, int B, int H, int N, int d,
+                       int transposed, fattn_stream_t stream) {
+  int rc = check_sizes(B, H, N, d);
+  if (rc != FATTN_OK) return rc;
+  if (d != 128) return FATTN_ERR_UNSUPPORTED;
+  if (!x || !codes || !scales) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u) != 0)
+    return FATTN_ERR_INVALID_ARG;
+  DeviceStatus* status = nullptr;
+  if ((rc = device_setup(&status)) != FATTN_OK) return rc;
+  return from_cuda(launch_fp8_quantize(x, codes, scales, B * H, N, d, transposed != 0,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fattn_fwd_fp8(const void* q8, const float* sq, const void* k8, const float* sk,
+                  const void* v8t, const float* sv, void* o, float* lse, int B, int H, int N,
+                  int d, int causal, float scale, fattn_stream_t stream) {
+  int rc = check_sizes(B, H, N, d);
+  if (rc != FATTN_OK) return rc;
+  if (d != 128) return FATTN_ERR_UNSUPPORTED;
+  if (!q8 || !sq || !k8 || !sk || !v8t || !sv || !o || !lse) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8t) || !aligned16(o) || !aligned16(lse))
+    return FATTN_ERR_INVALID_ARG;
+  for (const float* p : {sq, sk, sv})
+    if ((reinterpret_cast<uintptr_t>(p) & 3u) != 0) return FATTN_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return FATTN_ERR_INVALID_ARG;
+  DeviceStatus* status = nullptr;
+  if ((rc = device_setup(&status)) != FATTN_OK) return rc;
+  const int BH = B * H;
+  const int np = (N + 127) / 128 * 128;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_map_u8(&tq, q8, d, N, BH)) != FATTN_OK) return rc;
+  if ((rc = make_map_u8(&tk, k8, d, N, BH)) != FATTN_OK) return rc;
+  if ((rc = make_map_u8(&tv, v8t, np, d, BH)) != FATTN_OK) return rc;
+  FwdArgs a;
+  a.o = static_cast<uint16_t*>(o);
+  a.lse = lse;
+  a.status = status;
+  a.N = N;
+  a.BH = BH;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.sq = sq;
+  a.sk = sk;
+  a.sv = sv;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    a.wait_budget = g_budget;
+    a.tau_log2 = g_tau_log2;
+  }
+  return from_cuda(launch_fwd_fp8(causal != 0, tq, tk, tv, a,
+                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
 // Workspace of the backward pass: D and -L*log2(e) in a [B*H, Np] layout

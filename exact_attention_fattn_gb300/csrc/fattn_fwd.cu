@@ -48,12 +48,20 @@ constexpr int kCtrlRegs = 72;
 constexpr int kSoftmaxRegs = 216;
 static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs == kThreads * kLaunchRegs, "register split");
 
-template <int HD>
+// FP8: Q, K and the transposed V are e4m3 (one byte per element; d = 128
+// only), so a row of a tile is one 128-byte swizzle chunk and the ring holds
+// twice as many stages.
+template <int HD, bool FP8>
 struct FwdCfg {
-  static constexpr int kChunks = HD / 64;               // 128-byte swizzle chunks per row
+  static_assert(!FP8 || HD == 128, "the FP8 path is built for d = 128");
+  static constexpr int kElem = FP8 ? 1 : 2;             // bytes per element
+  static constexpr int kRowBytes = HD * kElem;
+  static constexpr int kChunks = kRowBytes / 128;       // 128-byte swizzle chunks per row
+  static constexpr int kChunkElems = 128 / kElem;
   static constexpr int kChunkBytes = kBM * 128;         // one chunk of a 128-row tile
-  static constexpr int kTileBytes = kBM * HD * 2;
-  static constexpr int kStages = HD == 128 ? 4 : 8;
+  static constexpr int kTileBytes = kBM * kRowBytes;
+  static constexpr int kKSteps = kRowBytes / 32;        // 32-byte K steps of Q K^T
+  static constexpr int kStages = FP8 ? 8 : (HD == 128 ? 4 : 8);
   static constexpr int kQOff = 0;
   static constexpr int kKvOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKvOff + kStages * kTileBytes;
@@ -65,7 +73,7 @@ struct FwdCfg {
   __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
   __device__ static constexpr uint32_t col_o(int t) { return 256u + HD * t; }
   __device__ static constexpr uint32_t col_p(int t) {
-    return HD == 128 ? 128u * t : 384u + 64u * t;
+    return (FP8 || HD == 128) ? 128u * t : 384u + 64u * t;
   }
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -101,11 +109,11 @@ __device__ __forceinline__ bool get_item(int m, int N, int BH, Item& w) {
   return true;
 }
 
-template <int HD, bool CAUSAL>
+template <int HD, bool CAUSAL, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
-  using C = FwdCfg<HD>;
+  using C = FwdCfg<HD, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -173,8 +181,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + C::col_s(t);
     const uint32_t tP = tmem + lane_off + C::col_p(t);
     const uint32_t tO = tmem + lane_off + C::col_o(t);
-    const float c = args.scale_log2;
+    float c = args.scale_log2;   // FP8: times the Q and K block scales, per tile pair
     const float tau = args.tau_log2;
+    const int n_kv = (N + kBN - 1) / kBN;
     uint32_t s_count = 0;   // S_t tiles consumed so far (phase of s_full / p_full)
     uint32_t o_count = 0;   // items of this tile finished so far (phase of o_full / o_empty)
     bool ok = true;
@@ -193,7 +202,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // which is exact for the dominating key.  (The other keys' rounding
       // errors stay, each weighted by its own small share of the row.)
       float l_fix = 0.f;
+      // FP8 ("FlashAttention v1～v4" v3 §3, block quantization): S = sq_i sk_j
+      // (Q8 K8^T), so the exponent multiplier is scale*log2e*sq_i*sk_j; V_j =
+      // sv_j V8_j is folded into the probabilities as rho_j = sv_j / sv_max
+      // (<= 1, so P rho stays within e4m3 range) and O is multiplied by
+      // sv_max once at the end.
+      float c_q = 0.f, sv_max = 1.f;
+      if constexpr (FP8) {
+        const float* svh = args.sv + static_cast<size_t>(w.bh) * n_kv;
+        sv_max = 0.f;
+        for (int jj = 0; jj < n_kv; ++jj) sv_max = fmaxf(sv_max, __ldg(svh + jj));
+        c_q = args.scale_log2 * __ldg(args.sq + static_cast<size_t>(w.bh) * n_kv + qs / kBM);
+      }
       for (int j = 0; j < nj; ++j) {
+        float rho = 1.f;
+        if constexpr (FP8) {
+          c = c_q * __ldg(args.sk + static_cast<size_t>(w.bh) * n_kv + j);
+          rho = __ldg(args.sv + static_cast<size_t>(w.bh) * n_kv + j) / sv_max;
+        }
         ok = __all_sync(0xffffffffu, mbar_wait(b.s_full[t], s_count & 1, wc, kWaitSFull));
         if (!ok) break;
         ++s_count;
@@ -264,13 +290,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           // the same arithmetic as the element loop below, for the largest score
           const float p_top = ex2_approx(fmaf(mx, c, -m_ref));
-          l_fix += __bfloat162float(__float2bfloat16_rn(p_top)) - p_top;
+          if constexpr (FP8)
+            l_fix += round_e4m3(p_top * rho) / rho - p_top;
+          else
+            l_fix += __bfloat162float(__float2bfloat16_rn(p_top)) - p_top;
         }
         const uint64_t c2 = splat2(c);
         const uint64_t nm2 = splat2(-m_ref);
         // Two columns per instruction (packed fp32 pairs); partial sums per
         // 32-column group keep the additions independent.
         uint64_t rs2[4];
+        const uint64_t rho2 = splat2(rho);
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           uint32_t pk[16];
@@ -281,10 +311,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             unpack2(ffma2(pack2(sv[g][2 * i], sv[g][2 * i + 1]), c2, nm2), x0, x1);
             const float a0 = ex2_approx(__uint_as_float(x0));
             const float a1 = ex2_approx(__uint_as_float(x1));
-            pk[i] = pack_bf16x2(a0, a1);
+            if constexpr (FP8)   // P rho, kept in the score registers until packed
+              unpack2(fmul2(pack2(__float_as_uint(a0), __float_as_uint(a1)), rho2), sv[g][2 * i],
+                      sv[g][2 * i + 1]);
+            else
+              pk[i] = pack_bf16x2(a0, a1);
             e2 = fadd2(e2, pack2(__float_as_uint(a0), __float_as_uint(a1)));
           }
-          tmem_st16(tP + 16 * g, pk);
+          if constexpr (FP8) {
+            // e4m3, four per TMEM column (K order), 8 columns per 32 keys
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              pk[q] = pack_e4m3x4(__uint_as_float(sv[g][4 * q]), __uint_as_float(sv[g][4 * q + 1]),
+                                  __uint_as_float(sv[g][4 * q + 2]),
+                                  __uint_as_float(sv[g][4 * q + 3]));
+            tmem_st8(tP + 8 * g, pk);
+          } else {
+            tmem_st16(tP + 16 * g, pk);
+          }
           rs2[g] = e2;
         }
         float rs[4];
@@ -307,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ++o_count;
       tc_fence_after();
-      const float inv = 1.f / (l + l_fix);
+      const float inv = sv_max / (l + l_fix);   // sv_max = 1 unless FP8
       const bool row_ok = row < N;
       uint4* orow = reinterpret_cast<uint4*>(args.o + (static_cast<size_t>(w.bh) * N +
                                                        (row_ok ? row : 0)) * HD);
@@ -339,36 +383,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ MMA issue
     // The whole warp runs this (converged); one elected lane issues.
     {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, HD, false, true);
+      constexpr uint32_t idesc_qk =
+          FP8 ? idesc_e4m3_f32(kBM, kBN) : idesc_bf16_f32(kBM, kBN, false, false);
+      constexpr uint32_t idesc_pv =
+          FP8 ? idesc_e4m3_f32(kBM, HD) : idesc_bf16_f32(kBM, HD, false, true);
       auto kv_smem = [&](uint32_t i) {
         return sbase + C::kKvOff + (i % C::kStages) * C::kTileBytes;
       };
       auto kv_full = [&](uint32_t i) { return b.kv_full0 + 8u * (i % C::kStages); };
       auto kv_empty = [&](uint32_t i) { return b.kv_empty0 + 8u * (i % C::kStages); };
       auto kv_parity = [&](uint32_t i) { return (i / C::kStages) & 1u; };
-      // S_t = Q_t K^T: M = 128, N = 128, K = HD in steps of 16 (32 bytes
-      // inside a 128-byte swizzle row, then the next 64-column chunk).  The
-      // descriptors are built once and advanced by constant offsets (their
-      // start-address field is in 16-byte units).
+      // S_t = Q_t K^T: M = 128, N = 128, K = HD in steps of 32 bytes (16
+      // bf16 or 32 e4m3 elements) inside a 128-byte swizzle row, then the
+      // next 128-byte chunk.  The descriptors are built once and advanced by
+      // constant offsets (their start-address field is in 16-byte units).
       auto issue_s = [&](int t, uint32_t ik) {
         const uint64_t da = sdesc_sw128(sbase + C::kQOff + t * C::kTileBytes, 16, 1024);
         const uint64_t db = sdesc_sw128(kv_smem(ik), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
+        for (int kk = 0; kk < C::kKSteps; ++kk) {
           const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-          mma_ss_w(tmem + C::col_s(t), da + off, db + off, idesc_qk, kk > 0 ? 1u : 0u);
+          if constexpr (FP8)
+            mma_ss_f8_w(tmem + C::col_s(t), da + off, db + off, idesc_qk, kk > 0 ? 1u : 0u);
+          else
+            mma_ss_w(tmem + C::col_s(t), da + off, db + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
-      // O_t += P_t V: A = P_t from TMEM (8 columns per K step of 16), B = V
-      // tile, MN-major (d contiguous): K step = 16 rows = 2048 bytes, the
-      // next 64 columns of d are one chunk (16 KiB) away.
+      // O_t += P_t V: A = P_t from TMEM (8 columns per K step: 16 bf16 or 32
+      // e4m3 keys).  bf16: B = the V tile, MN-major (d contiguous): K step =
+      // 16 rows = 2048 bytes, the next 64 columns of d one chunk (16 KiB)
+      // away.  FP8: B = the transposed V tile (d rows of 128 key bytes),
+      // K-major, K step = 32 bytes.
       auto issue_pv = [&](int t, uint32_t iv, uint32_t acc) {
-        const uint64_t dv = sdesc_sw128(kv_smem(iv), C::kChunkBytes, 1024);
+        if constexpr (FP8) {
+          const uint64_t dv = sdesc_sw128(kv_smem(iv), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts_w(tmem + C::col_o(t), tmem + C::col_p(t) + 8 * kk, dv + ((kk * 2048) >> 4),
-                   idesc_pv, kk > 0 ? 1u : acc);
+          for (int kk = 0; kk < kBN / 32; ++kk)
+            mma_ts_f8_w(tmem + C::col_o(t), tmem + C::col_p(t) + 8 * kk, dv + ((kk * 32) >> 4),
+                        idesc_pv, kk > 0 ? 1u : acc);
+        } else {
+          const uint64_t dv = sdesc_sw128(kv_smem(iv), C::kChunkBytes, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts_w(tmem + C::col_o(t), tmem + C::col_p(t) + 8 * kk, dv + ((kk * 2048) >> 4),
+                     idesc_pv, kk > 0 ? 1u : acc);
+        }
       };
       uint32_t kvb = 0;                      // ring index of this item's first K tile
       uint32_t p_count[2] = {0u, 0u};        // P_t tiles consumed (phase of p_full)
@@ -443,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (w.n[t] == 0) continue;
           for (int cc = 0; cc < C::kChunks; ++cc)
             tma_load_3d_w(sbase + C::kQOff + t * C::kTileBytes + cc * C::kChunkBytes, &tm_q,
-                          b.q_full, cc * 64, w.q0 + t * kBM, w.bh);
+                          b.q_full, cc * C::kChunkElems, w.q0 + t * kBM, w.bh);
         }
         items = m + 1;
         bool aborted = false;
@@ -461,8 +520,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx_w(full, C::kTileBytes);
           const CUtensorMap* tm = (i & 1) ? &tm_v : &tm_k;
           const uint32_t dst = sbase + C::kKvOff + s * C::kTileBytes;
-          for (int cc = 0; cc < C::kChunks; ++cc)
-            tma_load_3d_w(dst + cc * C::kChunkBytes, tm, full, cc * 64, (i >> 1) * kBN, w.bh);
+          if (FP8 && (i & 1)) {
+            // transposed V: d rows x 128 key bytes starting at key (i/2)*128
+            tma_load_3d_w(dst, tm, full, (i >> 1) * kBN, 0, w.bh);
+          } else {
+            for (int cc = 0; cc < C::kChunks; ++cc)
+              tma_load_3d_w(dst + cc * C::kChunkBytes, tm, full, cc * C::kChunkElems,
+                            (i >> 1) * kBN, w.bh);
+          }
         }
         if (aborted) break;
         kvb += 2 * w.nt;
@@ -487,11 +552,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int HD, bool CAUSAL>
+template <int HD, bool CAUSAL, bool FP8>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const FwdArgs& a, cudaStream_t stream) {
-  using C = FwdCfg<HD>;
-  auto kern = fwd_kernel<HD, CAUSAL>;
+  using C = FwdCfg<HD, FP8>;
+  auto kern = fwd_kernel<HD, CAUSAL, FP8>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -516,11 +581,17 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const FwdArgs& a, cudaStream_t stream) {
   if (d == 64) {
-    return causal ? launch_fwd_t<64, true>(tq, tk, tv, a, stream)
-                  : launch_fwd_t<64, false>(tq, tk, tv, a, stream);
+    return causal ? launch_fwd_t<64, true, false>(tq, tk, tv, a, stream)
+                  : launch_fwd_t<64, false, false>(tq, tk, tv, a, stream);
   }
-  return causal ? launch_fwd_t<128, true>(tq, tk, tv, a, stream)
-                : launch_fwd_t<128, false>(tq, tk, tv, a, stream);
+  return causal ? launch_fwd_t<128, true, false>(tq, tk, tv, a, stream)
+                : launch_fwd_t<128, false, false>(tq, tk, tv, a, stream);
+}
+
+cudaError_t launch_fwd_fp8(bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const FwdArgs& a, cudaStream_t stream) {
+  return causal ? launch_fwd_t<128, true, true>(tq, tk, tv, a, stream)
+                : launch_fwd_t<128, false, true>(tq, tk, tv, a, stream);
 }
 
 }  // namespace fattn

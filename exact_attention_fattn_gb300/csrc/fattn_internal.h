@@ -20,12 +20,27 @@ struct FwdArgs {
   int BH;
   float scale_log2;           // scale * log2(e)
   float tau_log2;             // rescale threshold (log2 units)
+  // FP8 only (nullptr otherwise): block scales [BH, ceil(N/128)] of Q, K, V
+  const float* sq;
+  const float* sk;
+  const float* sv;
 };
 
 // Launch the forward kernel for head dim d (64/128).  Tensor maps are 3-D
 // {d, N, B*H} views of q, k, v with 128-row boxes and a 128-byte swizzle.
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const FwdArgs& a, cudaStream_t stream);
+
+// FP8 forward (d = 128): tq, tk are 3-D uint8 views {d, N, B*H} of the e4m3
+// codes with 128-byte x 128-row boxes; tv a 3-D uint8 view {Np, d, B*H} of the
+// transposed V codes with the same box.
+cudaError_t launch_fwd_fp8(bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const FwdArgs& a, cudaStream_t stream);
+
+// Block quantization to e4m3: one scale per 128 rows of a head (amax / 448),
+// codes [BH, N, d] or, transposed, [BH, d, Np] with zero codes past N.
+cudaError_t launch_fp8_quantize(const void* x, void* codes, float* scales, int BH, int N, int d,
+                                bool transpose, cudaStream_t stream);
 
 struct BwdArgs {
   const float* L2;            // [BH, Np]: -lse * log2(e), -inf past N (Np = N rounded up to 128)

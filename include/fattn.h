@@ -63,6 +63,40 @@ int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
               fattn_stream_t stream);
 
 /*
+ * FP8 forward ("FlashAttention v1～v4" v3 §3: FP8 operands with block
+ * quantization).  d must be 128 (FATTN_ERR_UNSUPPORTED otherwise).
+ *
+ * fattn_quantize_fp8 turns a bf16 [B,H,N,d] tensor into e4m3 codes with one
+ * scale per 128 consecutive rows of a head (a block):
+ *   scale = amax(|x| over the block) / 448 (1 for an all-zero block),
+ *   code  = e4m3(x * (1 / scale)), rounded to nearest even and saturated at
+ *           +-448; the division, the reciprocal and the product are fp32.
+ *   x      : in,  bf16 [B,H,N,d], 16-byte aligned
+ *   codes  : out, uint8 [B,H,N,d], or with transposed != 0 uint8 [B,H,d,Np]
+ *            (Np = N rounded up to 128, zero codes for rows >= N); size from
+ *            fattn_fp8_codes_bytes; 16-byte aligned
+ *   scales : out, fp32 [B,H,ceil(N/128)]
+ * Q and K are quantized as they are, V transposed.  Returns a fattn_status.
+ *
+ * fattn_fwd_fp8 computes the forward pass of fattn_fwd on the dequantized
+ * inputs (code value x block scale), with both GEMMs on e4m3 operands and
+ * fp32 accumulation: S = sq_i sk_j (Q8 K8^T); the probabilities of key block
+ * j are multiplied by sv_j / max_j' sv_j' (at most 1) and rounded to e4m3 for
+ * P V, and O is rescaled once at the end; the row sums behind O's
+ * normalisation and L use the fp32 probabilities.
+ *   q8, k8  : in, uint8 [B,H,N,d] codes;   sq, sk: in, fp32 [B,H,ceil(N/128)]
+ *   v8t     : in, uint8 [B,H,d,Np] codes;  sv: in, fp32 [B,H,ceil(N/128)]
+ *   o, lse  : out, as for fattn_fwd
+ * Returns a fattn_status.
+ */
+size_t fattn_fp8_codes_bytes(int B, int H, int N, int d, int transposed);
+int fattn_quantize_fp8(const void* x, void* codes, float* scales, int B, int H, int N, int d,
+                       int transposed, fattn_stream_t stream);
+int fattn_fwd_fp8(const void* q8, const float* sq, const void* k8, const float* sk,
+                  const void* v8t, const float* sv, void* o, float* lse, int B, int H, int N,
+                  int d, int causal, float scale, fattn_stream_t stream);
+
+/*
  * Backward preprocessing: D_i = sum_k dO_ik * O_ik (fp32, one value per row;
  * the identity rowsum(dP o P) = rowsum(dO o O) of "6.1 FlashAttention
  * V1详解" §6.1), and zero the fp32 dQ accumulator.

@@ -1,0 +1,93 @@
+"""FP8 forward ("FlashAttention v1～v4" v3 §3): block quantization on the GPU
+bit for bit against the oracle's, and the FP8 forward against the exact
+attention of the dequantized inputs within the e4m3 bound."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_fattn_gb300 import attention as A
+from exact_attention_fattn_gb300 import workloads as W
+from gpu_util import to_np
+from tolerances import check_l, check_o_fp8
+
+pytestmark = pytest.mark.gpu
+
+
+def _quantize_all(inp):
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    q8, sq = A.fattn_quantize_fp8(q)
+    k8, sk = A.fattn_quantize_fp8(k)
+    v8t, sv = A.fattn_quantize_fp8(v, transposed=True)
+    assert A.fattn_check_status() == 0
+    return q8, sq, k8, sk, v8t, sv
+
+
+@pytest.mark.parametrize("B,H,N,outliers", [
+    (1, 2, 300, False), (2, 3, 128, False), (1, 1, 1, False), (1, 2, 1000, True),
+])
+def test_quantize_bit_exact(B, H, N, outliers):
+    w = W.Workload("q8", B, H, N, 128, False, seed=900 + N,
+                   outlier_frac=0.01 if outliers else 0.0, outlier_mult=20.0)
+    inp = W.make_inputs(w, with_grad=False)
+    if N >= 256:
+        inp["k"][0, 0, 128:256] = 0          # an all-zero block
+    q8, sq, k8, sk, v8t, sv = _quantize_all(inp)
+    for name, codes, scales, tr in (("q", q8, sq, False), ("k", k8, sk, False), ("v", v8t, sv, True)):
+        want_c, want_s = oracle.block_quantize(inp[name], transpose=tr)
+        assert np.array_equal(codes.cpu().numpy(), want_c), f"{name} codes differ"
+        assert np.array_equal(scales.cpu().numpy(), want_s), f"{name} scales differ"
+
+
+@pytest.mark.parametrize("B,H,N,causal,outliers", [
+    (1, 2, 256, False, False),
+    (1, 2, 300, True, False),
+    (2, 2, 640, True, True),
+    (1, 1, 1, False, False),
+    (1, 3, 1000, False, False),
+])
+def test_fwd_fp8_matches_reference(B, H, N, causal, outliers):
+    w = W.Workload("f8", B, H, N, 128, causal, seed=950 + N,
+                   outlier_frac=0.01 if outliers else 0.0, outlier_mult=20.0)
+    inp = W.make_inputs(w, with_grad=False)
+    q8, sq, k8, sk, v8t, sv = _quantize_all(inp)
+    o, lse = A.fattn_fwd_fp8(q8, sq, k8, sk, v8t, sv, causal=causal, scale=w.scale)
+    assert A.fattn_check_status() == 0
+    o_ref, l_ref = oracle.attention_fp8_reference(q8.cpu().numpy(), sq.cpu().numpy(),
+                                                  k8.cpu().numpy(), sk.cpu().numpy(),
+                                                  v8t.cpu().numpy(), sv.cpu().numpy(),
+                                                  causal, w.scale)
+    v_deq = oracle.block_dequantize(v8t.cpu().numpy(), sv.cpu().numpy(), N, transposed=True)
+    check_o_fp8(to_np(o), o_ref, float(np.abs(v_deq).max()))
+    check_l(to_np(lse), l_ref)
+
+
+def test_fwd_fp8_many_items_sampled_rows():
+    """Causal N = 4096 with the outlier rows (the benchmark's shape): several
+    work items per CTA; checked on 64 sampled rows per head."""
+    w = W.CAUSAL_OUTLIERS
+    inp = W.make_inputs(w, with_grad=False)
+    q8, sq, k8, sk, v8t, sv = _quantize_all(inp)
+    o, lse = A.fattn_fwd_fp8(q8, sq, k8, sk, v8t, sv, causal=True, scale=w.scale)
+    assert A.fattn_check_status() == 0
+    g = torch.Generator().manual_seed(4242)
+    rows = torch.randint(0, w.N, (w.B, w.H, 64), generator=g).numpy()
+    rows[:, :, 0] = 0
+    rows[:, :, 1] = w.N - 1
+    N = w.N
+    qd = oracle.block_dequantize(q8.cpu().numpy(), sq.cpu().numpy(), N)
+    kd = oracle.block_dequantize(k8.cpu().numpy(), sk.cpu().numpy(), N)
+    vd = oracle.block_dequantize(v8t.cpu().numpy(), sv.cpu().numpy(), N, transposed=True)
+    o_ref, l_ref = oracle.attention_forward_rows(qd, kd, vd, rows, True, w.scale)
+    o_np, l_np = to_np(o), to_np(lse)
+    o_got = np.stack([np.stack([o_np[b, h, rows[b, h]] for h in range(w.H)]) for b in range(w.B)])
+    l_got = np.stack([np.stack([l_np[b, h, rows[b, h]] for h in range(w.H)]) for b in range(w.B)])
+    check_o_fp8(o_got, o_ref, float(np.abs(vd).max()))
+    check_l(l_got, l_ref)
+
+
+def test_fp8_rejects_d64():
+    q = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):
+        A.fattn_quantize_fp8(q)

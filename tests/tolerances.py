@@ -50,3 +50,28 @@ def check_grad(g_gpu, g_ref, what):
     assert np.isfinite(g_gpu).all(), f"{what}: non-finite values"
     assert err <= GRAD_REL * ref_max, f"{what}: max err {err:.3e} > {GRAD_REL} * {ref_max:.3e}"
     return err / max(ref_max, 1e-30)
+
+
+# FP8 forward (e4m3 probabilities in P V): against the exact attention of the
+# dequantized inputs.  Every probability that meets V is rounded to e4m3 (3
+# mantissa bits, relative error <= 2^-4 with round to nearest); the row sum
+# that normalises O is taken on the unrounded values, so
+#   |O_fp8 - O_ref| <= 2^-4 * sum_k P_k |v_k| / l <= 2^-4 * max |V|
+# per element (subnormal codes, below 2^-6, err by at most 2^-10 absolute
+# each, far below this once weighted by P / l), plus the bf16 spacing of the
+# stored output.  With independent rounding errors the typical error is
+# ~2^-4 / sqrt(3) / sqrt(N_eff) * |V| (N_eff = keys that carry the row's
+# weight); the mean bound below, 1 % of max |V|, leaves a wide margin for rows
+# that few keys dominate.  L uses the fp32 probabilities and exact e4m3
+# products in S: the bf16 path's bound applies.
+FP8_O_MAX_REL, FP8_O_MEAN_REL = 2.0 ** -4, 1e-2
+
+
+def check_o_fp8(o_gpu, o_ref, v_absmax, what="O(fp8)"):
+    err = np.abs(o_gpu - o_ref)
+    allow = FP8_O_MAX_REL * v_absmax + bf16_spacing(o_ref)
+    worst = float((err - allow).max())
+    assert worst <= 0, f"{what}: max err {err.max():.3e} exceeds its bound (by {worst:.3e})"
+    assert err.mean() <= FP8_O_MEAN_REL * v_absmax, (
+        f"{what}: mean err {err.mean():.3e} > {FP8_O_MEAN_REL} * max|V| = {FP8_O_MEAN_REL * v_absmax:.3e}")
+    return float(err.max()), float(err.mean())
