@@ -392,6 +392,45 @@ def run_fattn(args, w):
         if A.fattn_check_status(dev) != 0:
             raise RuntimeError("libfattn reported an error in the end-to-end run")
 
+    # ---- extra rows, timed after the headline metric on the same inputs:
+    # the FP8 forward (block quantization of Q, K, V, then the e4m3 forward)
+    # and the deterministic backward.
+    extras = None
+    if not args.no_extras and w.d == 128:
+        def timed(fn, reps):
+            for _ in range(3):
+                fn()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            a0.record(stream)
+            for _ in range(reps):
+                fn()
+            a1.record(stream)
+            torch.cuda.synchronize(dev)
+            return a0.elapsed_time(a1) / reps
+
+        q8, sq = A.fattn_quantize_fp8(q)
+        k8, sk = A.fattn_quantize_fp8(k)
+        v8t, sv = A.fattn_quantize_fp8(v, transposed=True)
+        reps = max(3, min(args.steps, 50))
+        quant_ms = timed(lambda: (A.fattn_quantize_fp8(q), A.fattn_quantize_fp8(k),
+                                  A.fattn_quantize_fp8(v, transposed=True)), reps)
+        fp8_ms = timed(lambda: A.fattn_fwd_fp8(q8, sq, k8, sk, v8t, sv, causal=w.causal, scale=sc,
+                                               out=o, lse=lse), reps)
+        A.fattn_set_deterministic(True)
+        try:
+            det_ms = timed(lambda: A.fattn_bwd(q, k, v, o, do, lse, causal=w.causal, scale=sc,
+                                               workspace=ws, dq=dq, dk=dk, dv=dv), reps)
+        finally:
+            A.fattn_set_deterministic(False)
+        if A.fattn_check_status(dev) != 0:
+            raise RuntimeError("libfattn reported an error in the extra measurements")
+        base_x, bwd_x = flop_counts(w)
+        extras = {"fp8_fwd": {"tflops": base_x / (fp8_ms * 1e-3) / 1e12, "ms": fp8_ms,
+                              "quantize_qkv_ms": quant_ms, "steps": reps},
+                  "bwd_deterministic": {"tflops": bwd_x / (det_ms * 1e-3) / 1e12, "ms": det_ms,
+                                        "steps": reps}}
+
     if dist is not None:
         dist.destroy_process_group()
     if rank != 0:
@@ -434,6 +473,8 @@ def run_fattn(args, w):
         "gpu_launches": args.steps * len(stages),
         "e2e": e2e,
     }
+    if extras is not None:
+        line["extras"] = extras
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_heads)
     print(json.dumps(line), flush=True)
@@ -447,6 +488,8 @@ def main():
     ap.add_argument("--impl", choices=("fattn", "reference"), default="fattn")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the FP8 forward and deterministic backward measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-heads", type=int, default=32)
     args = ap.parse_args()
