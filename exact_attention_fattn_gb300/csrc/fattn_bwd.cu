@@ -598,18 +598,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               bulk_commit_group();
               bulk_wait_group_read1();
             }
-            if (qb == 1) {
+            if (qb == 1 && cnt == nullptr) {
               bulk_wait_group_read0();
               mbar_arrive(bar(kBarQEmpty + s));   // rows 0-63 (the Q half) read
             }
           }
           bulk_wait_group_read0();
-          mbar_arrive(bar(kBarDoEmpty + s));      // rows 64-127 (the dO half) read
           if (cnt != nullptr) {
             bulk_wait_group0();                   // the adds themselves have completed
             fence_proxy_async_global();
             st_release_gpu(cnt, static_cast<uint32_t>(w.j) + 1u);
+            // Only now is the stage handed back.  Released earlier, it could
+            // be refilled and two more dQ tiles parked while this warp waits
+            // for its adds; dQ-parked would then have completed two phases
+            // past the one this warp waits for next, and a parity wait
+            // cannot tell those apart.
+            mbar_arrive(bar(kBarQEmpty + s));
           }
+          mbar_arrive(bar(kBarDoEmpty + s));      // rows 64-127 (the dO half) read
         }
         __syncwarp();
       }

@@ -73,3 +73,30 @@ def test_deterministic_many_items_per_cta():
     dq_a, dq_f = a[0].float(), free[0].float()
     rel = ((dq_a - dq_f).abs().max() / dq_f.abs().max()).item()
     assert rel < 1e-2, rel
+
+
+def test_deterministic_repeats_on_the_benchmark_shape():
+    """Forty deterministic backward passes on the causal N = 4096 workload
+    (2048 items over the persistent grid): every one completes without a
+    wait timeout and all agree bit for bit."""
+    w = W.CAUSAL_OUTLIERS
+    inp = W.make_inputs(w)
+    o, lse = run_fwd(inp, True, w.scale)
+    ws = A.workspace_for(o)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    A.fattn_set_deterministic(True)
+    try:
+        ref = None
+        for it in range(40):
+            A.fattn_bwd(q, k, v, o, do, lse, causal=True, scale=w.scale, workspace=ws,
+                        dq=dq, dk=dk, dv=dv)
+            status = A.fattn_check_status()
+            assert status == 0, f"run {it}: status {status}"
+            if ref is None:
+                ref = (dq.clone(), dk.clone(), dv.clone())
+            else:
+                for a, b, name in zip((dq, dk, dv), ref, ("dQ", "dK", "dV")):
+                    assert torch.equal(a, b), f"run {it}: {name} differs"
+    finally:
+        A.fattn_set_deterministic(False)
