@@ -397,39 +397,13 @@ def run_fattn(args, w):
     # and the deterministic backward.
     extras = None
     if not args.no_extras and w.d == 128:
-        def timed(fn, reps):
-            for _ in range(3):
-                fn()
-            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize(dev)
-            a0.record(stream)
-            for _ in range(reps):
-                fn()
-            a1.record(stream)
-            torch.cuda.synchronize(dev)
-            return a0.elapsed_time(a1) / reps
-
-        q8, sq = A.fattn_quantize_fp8(q)
-        k8, sk = A.fattn_quantize_fp8(k)
-        v8t, sv = A.fattn_quantize_fp8(v, transposed=True)
-        reps = max(3, min(args.steps, 50))
-        quant_ms = timed(lambda: (A.fattn_quantize_fp8(q), A.fattn_quantize_fp8(k),
-                                  A.fattn_quantize_fp8(v, transposed=True)), reps)
-        fp8_ms = timed(lambda: A.fattn_fwd_fp8(q8, sq, k8, sk, v8t, sv, causal=w.causal, scale=sc,
-                                               out=o, lse=lse), reps)
-        A.fattn_set_deterministic(True)
         try:
-            det_ms = timed(lambda: A.fattn_bwd(q, k, v, o, do, lse, causal=w.causal, scale=sc,
-                                               workspace=ws, dq=dq, dk=dk, dv=dv), reps)
-        finally:
+            extras = measure_extras(args, w, (q, k, v, do), (o, lse), ws, (dq, dk, dv), dev,
+                                    stream)
+        except Exception as exc:   # the headline line must still be printed
             A.fattn_set_deterministic(False)
-        if A.fattn_check_status(dev) != 0:
-            raise RuntimeError("libfattn reported an error in the extra measurements")
-        base_x, bwd_x = flop_counts(w)
-        extras = {"fp8_fwd": {"tflops": base_x / (fp8_ms * 1e-3) / 1e12, "ms": fp8_ms,
-                              "quantize_qkv_ms": quant_ms, "steps": reps},
-                  "bwd_deterministic": {"tflops": bwd_x / (det_ms * 1e-3) / 1e12, "ms": det_ms,
-                                        "steps": reps}}
+            extras = {"error": f"{type(exc).__name__}: {exc}"}
+
 
     if dist is not None:
         dist.destroy_process_group()
@@ -479,6 +453,55 @@ def run_fattn(args, w):
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_heads)
     print(json.dumps(line), flush=True)
 
+
+
+def measure_extras(args, w, qkvd, out, ws, grads, dev, stream):
+    """Extra rows, timed after the headline metric on the same inputs: the FP8
+    forward (block quantization of Q, K, V, then the e4m3 forward) and the
+    deterministic backward."""
+    import torch
+
+    from exact_attention_fattn_gb300 import attention as A
+
+    q, k, v, do = qkvd
+    o, lse = out
+    dq, dk, dv = grads
+    sc = w.scale
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a0.record(stream)
+        for _ in range(reps):
+            fn()
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        return a0.elapsed_time(a1) / reps
+
+    q8, sq = A.fattn_quantize_fp8(q)
+    k8, sk = A.fattn_quantize_fp8(k)
+    v8t, sv = A.fattn_quantize_fp8(v, transposed=True)
+    reps = max(3, min(args.steps, 50))
+    quant_ms = timed(lambda: (A.fattn_quantize_fp8(q), A.fattn_quantize_fp8(k),
+                              A.fattn_quantize_fp8(v, transposed=True)), reps)
+    fp8_ms = timed(lambda: A.fattn_fwd_fp8(q8, sq, k8, sk, v8t, sv, causal=w.causal, scale=sc,
+                                           out=o, lse=lse), reps)
+    A.fattn_set_deterministic(True)
+    try:
+        det_ms = timed(lambda: A.fattn_bwd(q, k, v, o, do, lse, causal=w.causal, scale=sc,
+                                           workspace=ws, dq=dq, dk=dk, dv=dv), reps)
+    finally:
+        A.fattn_set_deterministic(False)
+    status = A.fattn_check_status(dev)
+    if status != 0:
+        raise RuntimeError(f"libfattn reported status {status} in the extra measurements")
+    base, bwd = flop_counts(w)
+    return {"fp8_fwd": {"tflops": base / (fp8_ms * 1e-3) / 1e12, "ms": fp8_ms,
+                        "quantize_qkv_ms": quant_ms, "steps": reps},
+            "bwd_deterministic": {"tflops": bwd / (det_ms * 1e-3) / 1e12, "ms": det_ms,
+                                  "steps": reps}}
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
