@@ -35,5 +35,6 @@ from .fp8 import (  # noqa: F401
     e4m3_encode,
     block_quantize,
     block_dequantize,
+    hadamard_rotate_fp32,
     attention_fp8_reference,
 )

@@ -18,7 +18,14 @@ reading taken here:
   rounded to fp32, then rounded to nearest e4m3 (ties to an even code) and
   saturated to +-448.  These steps decide an integer, so they are taken in
   fp32 as the kernel takes them;
-* the value a code stands for is decode(code) * scale (exact in fp64).
+* the value a code stands for is decode(code) * scale (exact in fp64);
+* incoherent processing (v3 §3: Q and K multiplied by one random orthogonal
+  matrix M before quantization, QM (KM)^T = Q K^T) uses the randomized
+  Hadamard transform M = diag(s) H / sqrt(d), H the Sylvester-Hadamard matrix
+  and s a caller-given vector of +-1 signs.  It is applied row by row in fp32
+  as the kernel applies it -- the signs, then the butterflies (a + b, a - b)
+  at strides 1, 2, 4, ..., d/2, then one multiplication by fp32(1/sqrt(d)) --
+  because its roundings decide the codes.
 
 ``attention_fp8_reference`` is the exact attention of the dequantized inputs
 (the plain definition, via ``attention_forward``): what an FP8 forward
@@ -73,14 +80,32 @@ def e4m3_encode(x) -> np.ndarray:
     return (code | np.where(sign, 0x80, 0)).astype(np.uint8)
 
 
-def block_quantize(x, transpose: bool = False):
-    """Quantize a [B, H, N, d] tensor block by block (128 rows of a head).
+def hadamard_rotate_fp32(x, signs) -> np.ndarray:
+    """x [..., d] (d a power of two) times diag(signs) H / sqrt(d), in fp32,
+    one rounding per butterfly, strides 1, 2, ..., d/2 in that order."""
+    y = np.asarray(x, dtype=np.float32) * np.asarray(signs, dtype=np.float32)
+    d = y.shape[-1]
+    h = 1
+    while h < d:
+        z = y.reshape(y.shape[:-1] + (d // (2 * h), 2, h))
+        a, b = z[..., 0, :], z[..., 1, :]
+        y = np.stack([(a + b).astype(np.float32), (a - b).astype(np.float32)],
+                     axis=-2).reshape(y.shape)
+        h *= 2
+    return (y * np.float32(1.0 / np.sqrt(d))).astype(np.float32)
+
+
+def block_quantize(x, transpose: bool = False, signs=None):
+    """Quantize a [B, H, N, d] tensor block by block (128 rows of a head),
+    after the randomized Hadamard rotation when ``signs`` is given.
 
     Returns (codes, scales): codes uint8 [B, H, N, d], or [B, H, d, Np] with Np
     = N rounded up to 128 and zero codes past N when ``transpose``; scales
     fp32 [B, H, ceil(N / 128)].
     """
     xf = np.asarray(to_f64(x), dtype=np.float32)
+    if signs is not None:
+        xf = hadamard_rotate_fp32(xf, signs)
     B, H, N, d = xf.shape
     nt = (N + BLOCK_ROWS - 1) // BLOCK_ROWS
     scales = np.empty((B, H, nt), dtype=np.float32)

@@ -117,9 +117,51 @@ def check_reference_on_exact_inputs(m):
     assert np.array_equal(o, o_ref) and np.array_equal(l, l_ref)
 
 
+def check_hadamard_basis_vectors(m):
+    """e_k -> s_k times row k of the Sylvester-Hadamard matrix (entries
+    (-1)^popcount(k & j)) over sqrt(d): every butterfly adds +-s_k to 0, so
+    the only rounding is the final fp32 multiplication."""
+    d = 128
+    rng = np.random.default_rng(21)
+    signs = rng.choice([-1.0, 1.0], d)
+    c = np.float32(1.0 / np.sqrt(d))
+    eye = np.eye(d, dtype=np.float32)
+    y = m.hadamard_rotate_fp32(eye, signs)
+    jj = np.arange(d)
+    for k in range(d):
+        parity = np.array([bin(k & j).count("1") & 1 for j in jj])
+        want = (np.float32(signs[k]) * np.where(parity, -1.0, 1.0).astype(np.float32) * c)
+        assert np.array_equal(y[k], want.astype(np.float32)), k
+
+
+def check_hadamard_matches_matrix(m):
+    """Random rows against the explicit product x diag(s) H / sqrt(d) in fp64
+    (H built by Kronecker products), and dot products preserved."""
+    d = 128
+    rng = np.random.default_rng(22)
+    signs = rng.choice([-1.0, 1.0], d)
+    H = np.array([[1.0]])
+    while H.shape[0] < d:
+        H = np.block([[H, H], [H, -H]])
+    x = (rng.standard_normal((64, d)) * 3).astype(np.float32)
+    want = (x.astype(np.float64) * signs) @ H / np.sqrt(d)
+    got = m.hadamard_rotate_fp32(x, signs).astype(np.float64)
+    assert np.abs(got - want).max() <= 1e-5 * np.abs(want).max()
+    q, k = x[:32], x[32:]
+    dots = q.astype(np.float64) @ k.astype(np.float64).T
+    dots_rot = got[:32] @ got[32:].T
+    assert np.abs(dots_rot - dots).max() <= 1e-4 * np.abs(dots).max()
+    # block_quantize with signs quantizes the rotated tensor
+    xt = x.reshape(1, 1, 64, d)
+    c1, s1 = m.block_quantize(xt, signs=signs)
+    c2, s2 = m.block_quantize(m.hadamard_rotate_fp32(xt, signs))
+    assert np.array_equal(c1, c2) and np.array_equal(s1, s2)
+
+
 ALL_FP8_CHECKS = [check_known_codes, check_table_monotone_and_round_trip, check_ties_to_even,
                   check_nearest, check_saturation, check_block_quantize,
-                  check_reference_on_exact_inputs]
+                  check_reference_on_exact_inputs, check_hadamard_basis_vectors,
+                  check_hadamard_matches_matrix]
 
 
 @pytest.mark.parametrize("check", ALL_FP8_CHECKS, ids=lambda c: c.__name__)
@@ -143,6 +185,12 @@ MUTATIONS = {
     "transpose_forgotten": ("out[:, :, :, :N] = codes.transpose(0, 1, 3, 2)",
                             "out[:, :, :, :N] = codes.reshape(B, H, d, N)"),
     "dequant_drops_scale": ("return vals * s[:, :, :, None]", "return vals"),
+    "hadamard_difference_swapped": ("(a - b).astype(np.float32)]", "(b - a).astype(np.float32)]"),
+    "hadamard_no_normalisation": ("return (y * np.float32(1.0 / np.sqrt(d))).astype(np.float32)",
+                                  "return y"),
+    "hadamard_signs_ignored": ("y = np.asarray(x, dtype=np.float32) * np.asarray(signs, dtype=np.float32)",
+                               "y = np.asarray(x, dtype=np.float32)"),
+    "hadamard_last_stage_skipped": ("    while h < d:", "    while h < d // 2:"),
 }
 
 
