@@ -28,6 +28,8 @@ SIGNATURES = {
                            _c_float, _vp]),
     "fattn_fp8_codes_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "fattn_quantize_fp8": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
+    "fattn_quantize_fp8_rotated": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                            _vp]),
     "fattn_fwd_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                _c_int, _c_int, _c_float, _vp]),
     "fattn_bwd_preprocess": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp]),

@@ -53,15 +53,33 @@ def fattn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=Non
     return o, l
 
 
-def fattn_quantize_fp8(x, transposed: bool = False):
+def fattn_quantize_fp8(x, transposed: bool = False, signs=None):
     """Block-quantize a bf16 [B,H,N,d] tensor (d = 128) to e4m3 codes.
 
     Returns (codes, scales): uint8 [B,H,N,d] (or [B,H,d,Np] when
     ``transposed``, Np = N rounded up to 128) and fp32 [B,H,ceil(N/128)].
+    With ``signs`` (fp32 CUDA tensor [d] of +-1) the rows are first rotated
+    by diag(signs) H / sqrt(d) (incoherent processing; for Q and K only).
     """
     _check_inputs([x])
     B, H, N, d = x.shape
     lib = _lib.load()
+    if signs is not None:
+        if transposed:
+            raise ValueError("the rotation applies to Q and K, which are not transposed")
+        if (signs.dtype != torch.float32 or not signs.is_cuda or signs.numel() != d
+                or not signs.is_contiguous()):
+            raise TypeError("signs must be a contiguous fp32 CUDA tensor of d values")
+        if d != 128:
+            raise ValueError("the FP8 path supports d = 128 only")
+        codes = torch.empty((B, H, N, d), dtype=torch.uint8, device=x.device)
+        scales = torch.empty((B, H, (N + 127) // 128), dtype=torch.float32, device=x.device)
+        with torch.cuda.device(x.device):
+            rc = lib.fattn_quantize_fp8_rotated(x.data_ptr(), signs.data_ptr(), codes.data_ptr(),
+                                                scales.data_ptr(), B, H, N, d,
+                                                _stream_ptr(x.device))
+        _lib.check("fattn_quantize_fp8_rotated", rc)
+        return codes, scales
     nbytes = int(lib.fattn_fp8_codes_bytes(B, H, N, d, int(bool(transposed))))
     if nbytes == 0:
         raise ValueError("the FP8 path supports d = 128 only")

@@ -188,6 +188,21 @@ int fattn_quantize_fp8(const void* x, void* codes, float* scales, int B, int H, 
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int fattn_quantize_fp8_rotated(const void* x, const float* signs, void* codes, float* scales,
+                               int B, int H, int N, int d, fattn_stream_t stream) {
+  int rc = check_sizes(B, H, N, d);
+  if (rc != FATTN_OK) return rc;
+  if (d != 128) return FATTN_ERR_UNSUPPORTED;
+  if (!x || !signs || !codes || !scales) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(signs) || !aligned16(codes) ||
+      (reinterpret_cast<uintptr_t>(scales) & 3u) != 0)
+    return FATTN_ERR_INVALID_ARG;
+  DeviceStatus* status = nullptr;
+  if ((rc = device_setup(&status)) != FATTN_OK) return rc;
+  return from_cuda(launch_fp8_quantize_rotated(x, signs, codes, scales, B * H, N, d,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int fattn_fwd_fp8(const void* q8, const float* sq, const void* k8, const float* sk,
                   const void* v8t, const float* sv, void* o, float* lse, int B, int H, int N,
                   int d, int causal, float scale, fattn_stream_t stream) {

@@ -42,6 +42,12 @@ cudaError_t launch_fwd_fp8(bool causal, const CUtensorMap& tq, const CUtensorMap
 cudaError_t launch_fp8_quantize(const void* x, void* codes, float* scales, int BH, int N, int d,
                                 bool transpose, cudaStream_t stream);
 
+// The same after the randomized Hadamard rotation diag(signs) H / sqrt(d) of
+// every row (d = 128; not transposed).
+cudaError_t launch_fp8_quantize_rotated(const void* x, const float* signs, void* codes,
+                                        float* scales, int BH, int N, int d,
+                                        cudaStream_t stream);
+
 struct BwdArgs {
   const float* L2;            // [BH, Np]: -lse * log2(e), -inf past N (Np = N rounded up to 128)
   const float* D;             // [BH, Np]: rowsum(dO o O), 0 past N

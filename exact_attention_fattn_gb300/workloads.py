@@ -8,8 +8,16 @@ Q, K, V (and dO when the workload has a backward pass) as fp32 standard
 normals of shape [B, H, N, d], each multiplied by ``value_scale``.  When
 ``outlier_frac`` > 0, for every (b, h) a set of round(outlier_frac * N) query
 rows and, independently, a set of key rows (both from ``torch.randperm`` on
-the same generator, Q first) are multiplied by ``outlier_mult``.  Finally
-every tensor is rounded to bf16 (round-to-nearest-even, torch ``.to``).
+the same generator, Q first) are multiplied by ``outlier_mult``.  When
+``entry_outlier_frac`` > 0, Q, K and V in turn draw a uniform [0, 1) tensor
+and a standard normal tensor of their shape; the entries whose uniform is
+below ``entry_outlier_frac`` are replaced by that normal times
+``entry_outlier_std`` (isolated large entries, the kind of outlier that
+block scales handle worst).  Finally every tensor is rounded to bf16
+(round-to-nearest-even, torch ``.to``).
+
+``random_signs`` draws the +-1 diagonal of the random orthogonal matrix used
+for incoherent processing before FP8 quantization.
 """
 
 from __future__ import annotations
@@ -34,6 +42,8 @@ class Workload:
     backward: bool = True
     seed: int = 1000
     check_rows: int = 0          # >0: the oracle checks this many rows per head
+    entry_outlier_frac: float = 0.0
+    entry_outlier_std: float = 1.0
 
     @property
     def scale(self) -> float:
@@ -76,7 +86,20 @@ def make_inputs(w: Workload, seed: int | None = None, with_grad: bool | None = N
                 for h in range(w.H):
                     rows = torch.randperm(w.N, generator=g)[:n_out]
                     t[name][b, h, rows] *= w.outlier_mult
+    if w.entry_outlier_frac > 0:
+        for name in ("q", "k", "v"):
+            u = torch.rand(shape, generator=g, dtype=torch.float32)
+            z = torch.randn(shape, generator=g, dtype=torch.float32) * w.entry_outlier_std
+            t[name] = torch.where(u < w.entry_outlier_frac, z, t[name])
     return {n: x.to(torch.bfloat16).contiguous() for n, x in t.items()}
+
+
+def random_signs(d: int, seed: int) -> torch.Tensor:
+    """fp32 [d] of +-1, each sign an independent fair draw (CPU tensor)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    bits = torch.randint(0, 2, (d,), generator=g)
+    return (bits * 2 - 1).to(torch.float32)
 
 
 def sample_rows(w: Workload, count: int, seed: int, causal_spread: bool = True):

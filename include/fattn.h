@@ -92,6 +92,22 @@ int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 size_t fattn_fp8_codes_bytes(int B, int H, int N, int d, int transposed);
 int fattn_quantize_fp8(const void* x, void* codes, float* scales, int B, int H, int N, int d,
                        int transposed, fattn_stream_t stream);
+
+/*
+ * Incoherent processing ("FlashAttention v1～v4" v3 §3): quantize x M instead
+ * of x, M = diag(signs) H / sqrt(d) with H the Sylvester-Hadamard matrix, an
+ * orthogonal matrix, so quantizing Q M and K M leaves S = Q K^T unchanged in
+ * exact arithmetic while an outlier's energy is spread over all d columns
+ * before the block scale is taken.  Each row is rotated in fp32 (the signs,
+ * butterflies a + b / a - b at strides 1, 2, ..., 64, then one multiplication
+ * by fp32(1/sqrt(d))), then quantized as by fattn_quantize_fp8 (not
+ * transposed).  Apply it to Q and K with the same signs, never to V.
+ *   signs : in, fp32 [d] of +1 / -1, 16-byte aligned (only the sign bit of
+ *           each entry is read)
+ * Other arguments as for fattn_quantize_fp8; d must be 128.
+ */
+int fattn_quantize_fp8_rotated(const void* x, const float* signs, void* codes, float* scales,
+                               int B, int H, int N, int d, fattn_stream_t stream);
 int fattn_fwd_fp8(const void* q8, const float* sq, const void* k8, const float* sk,
                   const void* v8t, const float* sv, void* o, float* lse, int B, int H, int N,
                   int d, int causal, float scale, fattn_stream_t stream);
