@@ -314,6 +314,7 @@ def run_fattn(args, w):
     t_host1 = time.time()
     barrier(dist)
     total_ms = max_over_ranks(start.elapsed_time(end), dist, dev)
+    step_times = [ev[s][0].elapsed_time(ev[s][len(stages)]) for s in range(args.steps)]
     status = A.fattn_check_status(dev)
     if status != 0:
         raise RuntimeError(f"libfattn reported status {status} in the timed region")
@@ -403,6 +404,10 @@ def run_fattn(args, w):
         except Exception as exc:   # the headline line must still be printed
             A.fattn_set_deterministic(False)
             extras = {"error": f"{type(exc).__name__}: {exc}"}
+        try:
+            extras["sweep"] = measure_sweep(dev)
+        except Exception as exc:
+            extras["sweep"] = {"error": f"{type(exc).__name__}: {exc}"}
 
 
     if dist is not None:
@@ -442,6 +447,10 @@ def run_fattn(args, w):
         "fwd_tflops": fwd_tf, "fwd_frac_of_peak": fwd_tf / peaks["bf16"],
         "bwd_tflops": bwd_tf,
         "stage_ms": per_stage,
+        "step_ms": {"mean": ms_step, "median": statistics.median(step_times),
+                    "min": min(step_times)},
+        "frac_of_spec_peak": value / world / spec_tflops(dev, clocks),
+        "frac_of_spec_peak_note": "per-GPU value / (SMs x 8192 FLOP/clk/SM x max SM clock)",
         "roofline": roofline,
         "clocks": clocks,
         "gpu_launches": args.steps * len(stages),
@@ -453,6 +462,88 @@ def run_fattn(args, w):
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_heads)
     print(json.dumps(line), flush=True)
 
+
+
+def spec_tflops(dev, clocks):
+    """SMs x 8192 dense bf16 FLOP per clock per SM x the maximum SM clock."""
+    import torch
+
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = (clocks or {}).get("sm_max_mhz") or 2070.0
+    return sms * 8192.0 * float(mhz) * 1e6 / 1e12
+
+
+# The workloads besides the headline one, timed per call: (name, B, H, N, d,
+# causal, value scale, with backward).  The non-causal N = 4096 points use the
+# batch and heads of the sweep workload and of the headline workload.
+SWEEP = (
+    ("tiny_b1h1_n128_d64", 1, 1, 128, 64, False, 1.0, False),
+    ("b4h16_n1024_d64", 4, 16, 1024, 64, False, 1.0, True),
+    ("b8h16_n512_d128_half", 8, 16, 512, 128, False, 0.5, False),
+    ("b8h16_n1024_d128_half", 8, 16, 1024, 128, False, 0.5, False),
+    ("b8h16_n2048_d128_half", 8, 16, 2048, 128, False, 0.5, False),
+    ("b8h16_n4096_d128", 8, 16, 4096, 128, False, 1.0, True),
+    ("b2h32_n4096_d128", 2, 32, 4096, 128, False, 1.0, True),
+    ("b1h16_n16384_d128_causal", 1, 16, 16384, 128, True, 1.0, True),
+)
+
+
+def measure_sweep(dev, warmup=5, reps=20):
+    """Forward (and backward) TFLOP/s of every workload besides the headline:
+    inputs drawn on the device (timing only), 5 warm-up calls, then 20 calls
+    each between CUDA events; median and best.  The tiny workload is bound by
+    the host's call rate, not by the kernel."""
+    import torch
+
+    from exact_attention_fattn_gb300 import attention as A
+
+    g = torch.Generator(device=dev)
+    out = []
+    for name, B, H, N, d, causal, vs, with_bwd in SWEEP:
+        g.manual_seed(2000 + len(out))
+        q, k, v, do = (
+            (torch.randn((B, H, N, d), generator=g, device=dev) * vs).to(torch.bfloat16)
+            for _ in range(4))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        sc = A.default_scale(d)
+        fl = 4.0 * B * H * N * N * d * (0.5 if causal else 1.0)
+
+        def per_call(fn):
+            for _ in range(warmup):
+                fn()
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+            torch.cuda.synchronize(dev)
+            evs[0].record()
+            for i in range(reps):
+                fn()
+                evs[i + 1].record()
+            torch.cuda.synchronize(dev)
+            ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(reps)]
+            return statistics.median(ms), min(ms)
+
+        fwd_med, fwd_min = per_call(
+            lambda: A.fattn_fwd(q, k, v, causal=causal, scale=sc, out=o, lse=lse))
+        row = {"workload": name, "fwd_ms_median": fwd_med,
+               "fwd_tflops_median": fl / (fwd_med * 1e-3) / 1e12,
+               "fwd_tflops_best": fl / (fwd_min * 1e-3) / 1e12}
+        if with_bwd:
+            ws = A.workspace_for(q)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            bwd_med, bwd_min = per_call(
+                lambda: A.fattn_bwd(q, k, v, o, do, lse, causal=causal, scale=sc, workspace=ws,
+                                    dq=dq, dk=dk, dv=dv))
+            row.update({"bwd_ms_median": bwd_med,
+                        "bwd_tflops_median": 2.5 * fl / (bwd_med * 1e-3) / 1e12,
+                        "bwd_tflops_best": 2.5 * fl / (bwd_min * 1e-3) / 1e12})
+            del ws, dq, dk, dv
+        status = A.fattn_check_status(dev)
+        if status != 0:
+            raise RuntimeError(f"libfattn reported status {status} on {name}")
+        out.append(row)
+        del q, k, v, do, o, lse
+        torch.cuda.empty_cache()
+    return out
 
 
 def measure_extras(args, w, qkvd, out, ws, grads, dev, stream):
@@ -539,7 +630,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the FP8 forward and deterministic backward measurements")
+                    help="skip the FP8 forward, deterministic backward and workload sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-heads", type=int, default=32)
     args = ap.parse_args()

@@ -120,20 +120,46 @@ enum : int {
 // The m-th work item of this CTA: K/V tile j of head bh, with the Q tiles
 // i0 .. n_tiles-1.  Items are numbered heaviest first (k = j * BH + bh) and
 // dealt in snake order.  Returns false past the last item.
+// A work item: K/V tile j of head bh, walking n_it Q tiles.  Step it visits
+// Q tile qtile(it): i0 + it (causal: i0 = j), or, without a mask and without
+// the ordered dQ reduction, (j + it) mod n_tiles, so that the K/V tiles of one
+// head start on different Q tiles instead of all reduce-adding into tile 0.
 struct BwdItem {
-  int j, bh, i0, n_it;
+  int j, bh, i0, n_it, rot;
 };
 
 template <bool CAUSAL>
-__device__ __forceinline__ bool get_bwd_item(int m, int n_tiles, int BH, BwdItem& w) {
+__device__ __forceinline__ int qtile(const BwdItem& w, int it, int n_tiles) {
+  if constexpr (CAUSAL) {
+    return w.i0 + it;
+  } else {
+    const int i = it + w.rot;
+    return i >= n_tiles ? i - n_tiles : i;
+  }
+}
+
+// Items are numbered in sections of sec_heads heads (sized so that a
+// section's dQ accumulator, Q, dO, L and D stay in L2 while its items run)
+// and, inside a section, heaviest first: by j (causal: K/V tile j has
+// n_tiles - j Q tiles), heads inner.  The m-th item of this CTA is dealt in
+// snake order over the CTAs.
+template <bool CAUSAL>
+__device__ __forceinline__ bool get_bwd_item(int m, int n_tiles, const BwdArgs& a, BwdItem& w) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   const long long k = static_cast<long long>(m) * G + ((m & 1) ? (G - 1 - c) : c);
-  if (k >= static_cast<long long>(n_tiles) * BH) return false;
+  if (k >= static_cast<long long>(n_tiles) * a.BH) return false;
+  // item counts fit in int (the launcher checks n_tiles * BH < 2^31)
   const int kk = static_cast<int>(k);
-  w.j = kk / BH;
-  w.bh = kk % BH;
+  const int sec_items = a.sec_heads * n_tiles;
+  const int sec = kk / sec_items;
+  const int kp = kk - sec * sec_items;
+  const int h0 = sec * a.sec_heads;
+  const int hs = min(a.sec_heads, a.BH - h0);
+  w.j = kp / hs;
+  w.bh = h0 + kp % hs;
   w.i0 = CAUSAL ? w.j : 0;
   w.n_it = n_tiles - w.i0;
+  w.rot = (!CAUSAL && a.dq_order == nullptr) ? w.j : 0;
   return true;
 }
 
@@ -216,12 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     uint32_t step = 0;                       // steps done by this CTA (all items)
     BwdItem w;
-    for (int m = 0; ok && get_bwd_item<CAUSAL>(m, n_tiles, BH, w); ++m) {
+    for (int m = 0; ok && get_bwd_item<CAUSAL>(m, n_tiles, args, w); ++m) {
       const int kv0 = w.j * kTile;
       const int kv = kv0 + r;
       const bool kv_valid = kv < N;
       for (int it = 0; it < w.n_it; ++it, ++step) {
-        const int i = w.i0 + it;
+        const int i = qtile<CAUSAL>(w, it, n_tiles);
         const int q0 = i * kTile;
         const int s = step & 1;
         const uint32_t ph = step & 1;
@@ -401,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       uint32_t step = 0;                     // steps issued by this CTA (all items)
       BwdItem w;
-      for (int m = 0; get_bwd_item<CAUSAL>(m, n_tiles, BH, w); ++m) {
+      for (int m = 0; get_bwd_item<CAUSAL>(m, n_tiles, args, w); ++m) {
         const int n_it = w.n_it;
         const uint32_t s0 = step & 1;
         const uint32_t sK = sbase + C::kv_off(m, 0), sV = sbase + C::kv_off(m, 1);
@@ -490,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load_step = [&](const BwdItem& wi, int it) -> bool {
         const int s = step & 1;
         const uint32_t rnd = step >> 1;
-        const int q0 = (wi.i0 + it) * kTile;
+        const int q0 = qtile<CAUSAL>(wi, it, n_tiles) * kTile;
         const uint32_t dst = sbase + C::kStageOff + s * C::kStageBytes;
         if (rnd > 0 && !mbar_wait_warp(bar(kBarQEmpty + s), (rnd - 1) & 1, wc, kWaitKvEmpty))
           return false;
@@ -513,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++step;
         return true;
       };
-      for (int m = 0; ok && get_bwd_item<CAUSAL>(m, n_tiles, BH, w); ++m) {
+      for (int m = 0; ok && get_bwd_item<CAUSAL>(m, n_tiles, args, w); ++m) {
         const int kv0 = w.j * kTile;
         // K_j goes where the previous item's V was, V_j where its K was.
         if (m > 0 && !mbar_wait_warp(bar(kBarVEmpty), (m - 1) & 1, wc, kWaitKvEmpty)) break;
@@ -531,12 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         items_v = m + 1;
         for (int it = 1; it < w.n_it && ok; ++it) ok = load_step(w, it);
         BwdItem wn;
-        if (ok && get_bwd_item<CAUSAL>(m + 1, n_tiles, BH, wn)) {
+        if (ok && get_bwd_item<CAUSAL>(m + 1, n_tiles, args, wn)) {
           for (int cc = 0; cc < C::kChunks; ++cc) {
             tma_prefetch_l2_3d_w(&tm_k, cc * 64, wn.j * kTile, wn.bh);
             tma_prefetch_l2_3d_w(&tm_v, cc * 64, wn.j * kTile, wn.bh);
-            tma_prefetch_l2_3d_w(&tm_q, cc * 64, wn.i0 * kTile, wn.bh);
-            tma_prefetch_l2_3d_w(&tm_do, cc * 64, wn.i0 * kTile, wn.bh);
+            tma_prefetch_l2_3d_w(&tm_q, cc * 64, qtile<CAUSAL>(wn, 0, n_tiles) * kTile, wn.bh);
+            tma_prefetch_l2_3d_w(&tm_do, cc * 64, qtile<CAUSAL>(wn, 0, n_tiles) * kTile, wn.bh);
           }
         }
       }
@@ -563,15 +589,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     uint32_t step = 0;
     BwdItem w;
-    for (int m = 0; ok && get_bwd_item<CAUSAL>(m, n_tiles, BH, w); ++m) {
+    for (int m = 0; ok && get_bwd_item<CAUSAL>(m, n_tiles, args, w); ++m) {
       for (int it = 0; it < w.n_it; ++it, ++step) {
         const int s = step & 1;
-        const int q0 = (w.i0 + it) * kTile;
+        const int qt = qtile<CAUSAL>(w, it, n_tiles);
+        const int q0 = qt * kTile;
         const int bh = w.bh;
         ok = mbar_wait_warp(bar(kBarDqEmpty), step & 1, wc, kWaitDqEmpty);
         if (!ok) break;
         uint32_t* const cnt =
-            order != nullptr ? order + static_cast<size_t>(bh) * n_tiles + (w.i0 + it) : nullptr;
+            order != nullptr ? order + static_cast<size_t>(bh) * n_tiles + qt : nullptr;
         if (cnt != nullptr) {
           bool turn = true;
           if (lane == 0) {
@@ -634,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     uint32_t step = 0;
     BwdItem w;
-    for (int m = 0; ok && get_bwd_item<CAUSAL>(m, n_tiles, BH, w); ++m) {
+    for (int m = 0; ok && get_bwd_item<CAUSAL>(m, n_tiles, args, w); ++m) {
       for (int it = 0; it < w.n_it; ++it, ++step) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDqFull), step & 1, wc, kWaitDqFull));
         if (!ok) break;
@@ -692,10 +719,29 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
+  int l2 = 0;
+  if ((e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev)) != cudaSuccess) return e;
   // Persistent grid: one CTA per SM (at most one per work item).
-  const long long items = static_cast<long long>((a.N + kTile - 1) / kTile) * a.BH;
+  const int n_tiles = (a.N + kTile - 1) / kTile;
+  const long long items = static_cast<long long>(n_tiles) * a.BH;
+  if (items >= 0x7fffffffLL) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(items < sms ? items : sms));
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tacc, a);
+  // Heads per section: a third of L2 over what one head's steps keep
+  // re-reading (fp32 dQ accumulator, Q, dO, L, D).  Only without a mask and
+  // without the ordered reduction: causal items of one head (and, in the
+  // ordered mode, any items of one head) meet on the same Q tiles one step
+  // apart, and the more of them run at once the more they wait on each
+  // other, which costs more than the L2 misses that sections avoid
+  // (measured on GB300: causal backward 15 % slower, ordered 1.8x slower).
+  BwdArgs ab = a;
+  ab.sec_heads = a.BH;
+  if (!CAUSAL && a.dq_order == nullptr) {
+    const long long per_head =
+        static_cast<long long>(n_tiles) * kTile * (HD * 4 + 2 * HD * 2 + 2 * 4);
+    const long long fit = per_head > 0 ? (static_cast<long long>(l2) / 3) / per_head : 1;
+    ab.sec_heads = static_cast<int>(fit < 1 ? 1 : (fit > a.BH ? a.BH : fit));
+  }
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tacc, ab);
   return cudaGetLastError();
 }
 

@@ -59,6 +59,7 @@ struct BwdArgs {
   long long wait_budget;
   int N;
   int BH;
+  int sec_heads;              // heads per scheduling section (set by the launcher)
   float scale;
   float scale_log2;
 };
