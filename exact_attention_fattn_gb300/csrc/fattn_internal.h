@@ -18,6 +18,7 @@ struct FwdArgs {
   long long wait_budget;      // cycles
   int N;
   int BH;
+  int sec_heads;              // heads per scheduling section (set by the launcher)
   float scale_log2;           // scale * log2(e)
   float tau_log2;             // rescale threshold (log2 units)
   // FP8 only (nullptr otherwise): block scales [BH, ceil(N/128)] of Q, K, V
