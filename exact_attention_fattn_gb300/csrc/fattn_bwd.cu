@@ -143,9 +143,33 @@ __device__ __forceinline__ int qtile(const BwdItem& w, int it, int n_tiles) {
 // and, inside a section, heaviest first: by j (causal: K/V tile j has
 // n_tiles - j Q tiles), heads inner.  The m-th item of this CTA is dealt in
 // snake order over the CTAs.
+//
+// Causal with paired items (a.paired: even n_tiles, any-order dQ): the CTA's
+// items 2q and 2q + 1 are K/V tiles p and n_tiles - 1 - p of one head, the
+// q-th pair dealt to it, so every pair walks n_tiles + 1 Q tiles and the pairs
+// can be numbered in head sections without unbalancing the CTAs.
 template <bool CAUSAL>
 __device__ __forceinline__ bool get_bwd_item(int m, int n_tiles, const BwdArgs& a, BwdItem& w) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  if (CAUSAL && a.paired) {
+    const int n_pairs = n_tiles >> 1;
+    const int q = m >> 1;
+    const long long k = static_cast<long long>(q) * G + ((q & 1) ? (G - 1 - c) : c);
+    if (k >= static_cast<long long>(n_pairs) * a.BH) return false;
+    const int kk = static_cast<int>(k);
+    const int sec_items = a.sec_heads * n_pairs;
+    const int sec = kk / sec_items;
+    const int kp = kk - sec * sec_items;
+    const int h0 = sec * a.sec_heads;
+    const int hs = min(a.sec_heads, a.BH - h0);
+    const int p = kp / hs;
+    w.bh = h0 + kp % hs;
+    w.j = (m & 1) ? n_tiles - 1 - p : p;
+    w.i0 = w.j;
+    w.n_it = n_tiles - w.i0;
+    w.rot = 0;
+    return true;
+  }
   const long long k = static_cast<long long>(m) * G + ((m & 1) ? (G - 1 - c) : c);
   if (k >= static_cast<long long>(n_tiles) * a.BH) return false;
   // item counts fit in int (the launcher checks n_tiles * BH < 2^31)
@@ -727,15 +751,15 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   if (items >= 0x7fffffffLL) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(items < sms ? items : sms));
   // Heads per section: a third of L2 over what one head's steps keep
-  // re-reading (fp32 dQ accumulator, Q, dO, L, D).  Only without a mask and
-  // without the ordered reduction: causal items of one head (and, in the
-  // ordered mode, any items of one head) meet on the same Q tiles one step
-  // apart, and the more of them run at once the more they wait on each
-  // other, which costs more than the L2 misses that sections avoid
-  // (measured on GB300: causal backward 15 % slower, ordered 1.8x slower).
+  // re-reading (fp32 dQ accumulator, Q, dO, L, D).  Not with the ordered
+  // reduction: there the items of a head wait on each other at every Q tile,
+  // and the more of them run at once the longer the chains (measured on
+  // GB300: 1.8x slower).  Causal items are paired first (equal weights), or
+  // keep the all-heads heaviest-first order when n_tiles is odd.
   BwdArgs ab = a;
   ab.sec_heads = a.BH;
-  if (!CAUSAL && a.dq_order == nullptr) {
+  ab.paired = CAUSAL && a.dq_order == nullptr && (n_tiles % 2) == 0 ? 1 : 0;
+  if ((!CAUSAL || ab.paired) && a.dq_order == nullptr) {
     const long long per_head =
         static_cast<long long>(n_tiles) * kTile * (HD * 4 + 2 * HD * 2 + 2 * 4);
     const long long fit = per_head > 0 ? (static_cast<long long>(l2) / 3) / per_head : 1;

@@ -61,6 +61,7 @@ struct BwdArgs {
   int N;
   int BH;
   int sec_heads;              // heads per scheduling section (set by the launcher)
+  int paired;                 // causal K/V tiles p and n - 1 - p paired (set by the launcher)
   float scale;
   float scale_log2;
 };
