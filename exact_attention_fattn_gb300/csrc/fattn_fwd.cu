@@ -224,10 +224,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         c_q = args.scale_log2 * __ldg(args.sq + static_cast<size_t>(w.bh) * n_kv + qs / kBM);
       }
       for (int j = 0; j < nj; ++j) {
-        float rho = 1.f;
+        // FP8: rho_j enters the exponent as log2(rho_j) (one FMA gives P rho),
+        // and the row sum is taken of P rho and multiplied by 1/rho_j.  The
+        // offset is clamped at -100: probabilities scaled further down round
+        // to e4m3 zero either way, and the sum stays finite.
+        float lrho = 0.f, inv_rho = 1.f;
         if constexpr (FP8) {
           c = c_q * __ldg(args.sk + static_cast<size_t>(w.bh) * n_kv + j);
-          rho = __ldg(args.sv + static_cast<size_t>(w.bh) * n_kv + j) / sv_max;
+          const float rho = __ldg(args.sv + static_cast<size_t>(w.bh) * n_kv + j) / sv_max;
+          lrho = fmaxf(__log2f(rho), -100.f);
+          inv_rho = ex2_approx(-lrho);
         }
         ok = __all_sync(0xffffffffu, mbar_wait(b.s_full[t], s_count & 1, wc, kWaitSFull));
         if (!ok) break;
@@ -296,20 +302,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        // exponent offset of the element loop: -m_ref, and log2(rho_j) for FP8
+        const float nm = FP8 ? -m_ref + lrho : -m_ref;
         {
           // the same arithmetic as the element loop below, for the largest score
           const float p_top = ex2_approx(fmaf(mx, c, -m_ref));
           if constexpr (FP8)
-            l_fix += round_e4m3(p_top * rho) / rho - p_top;
+            l_fix += round_e4m3(ex2_approx(fmaf(mx, c, nm))) * inv_rho - p_top;
           else
             l_fix += __bfloat162float(__float2bfloat16_rn(p_top)) - p_top;
         }
         const uint64_t c2 = splat2(c);
-        const uint64_t nm2 = splat2(-m_ref);
+        const uint64_t nm2 = splat2(nm);
         // Two columns per instruction (packed fp32 pairs); partial sums per
         // 32-column group keep the additions independent.
         uint64_t rs2[4];
-        const uint64_t rho2 = splat2(rho);
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           uint32_t pk[16];
@@ -320,11 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             unpack2(ffma2(pack2(sv[g][2 * i], sv[g][2 * i + 1]), c2, nm2), x0, x1);
             const float a0 = ex2_approx(__uint_as_float(x0));
             const float a1 = ex2_approx(__uint_as_float(x1));
-            if constexpr (FP8)   // P rho, kept in the score registers until packed
-              unpack2(fmul2(pack2(__float_as_uint(a0), __float_as_uint(a1)), rho2), sv[g][2 * i],
-                      sv[g][2 * i + 1]);
-            else
+            if constexpr (FP8) {   // P rho, kept in the score registers until packed
+              sv[g][2 * i] = __float_as_uint(a0);
+              sv[g][2 * i + 1] = __float_as_uint(a1);
+            } else {
               pk[i] = pack_bf16x2(a0, a1);
+            }
             e2 = fadd2(e2, pack2(__float_as_uint(a0), __float_as_uint(a1)));
           }
           if constexpr (FP8) {
@@ -347,7 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           unpack2(rs2[g], u0, u1);
           rs[g] = __uint_as_float(u0) + __uint_as_float(u1);
         }
-        l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+        if constexpr (FP8)
+          l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) * inv_rho;
+        else
+          l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(b.p_full[t]);
