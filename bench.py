@@ -183,7 +183,7 @@ def cpu_baseline(w, heads: int):
     import oracle
     from exact_attention_fattn_gb300 import workloads as W
 
-    inp = W.make_inputs(w)
+    inp = W.make_inputs(w, with_grad=True)
     base, bwd = flop_counts(w)
     per_head = (base + bwd) / (w.B * w.H)
     t0 = time.perf_counter()
@@ -208,7 +208,7 @@ def run_reference(args, w):
     import oracle
     from exact_attention_fattn_gb300 import workloads as W
 
-    inp = W.make_inputs(w)
+    inp = W.make_inputs(w, with_grad=True)
     base, bwd = flop_counts(w)
     per_head = (base + bwd) / (w.B * w.H)
     nheads = w.B * w.H
@@ -261,7 +261,7 @@ def run_fattn(args, w):
     torch.cuda.set_device(dev)
 
     # replicas only: each rank draws its own batch of the same workload
-    inp = W.make_inputs(w, seed=replica_seed(w.seed, rank))
+    inp = W.make_inputs(w, seed=replica_seed(w.seed, rank), with_grad=True)
     q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
