@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -61,8 +62,14 @@ def load_peaks():
 
 
 def source_hash(rel):
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256[:16] of a kernel source with its comments and whitespace
+    removed, so that only a change to the code invalidates a capture."""
+    with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    src = re.sub(r"\s+", "", src)
+    return hashlib.sha256(src.encode("utf-8")).hexdigest()[:16]
 
 
 def load_traffic(kernel, workload):

@@ -14,8 +14,8 @@
 // from S = scale Q K^T by the chain rule (the pages stop at dS).
 //
 // Persistent ("FlashAttention v1～v4" v4 §4 scheduling): one CTA per SM walks
-// items numbered heaviest first (causal: small j has the most Q tiles) and
-// dealt in snake order.  The Q/dO ring and every per-step barrier run on one
+// items numbered heaviest first (causal: small j has the most Q tiles) in
+// L2-sized head sections and dealt in snake order (see get_bwd_item).  The Q/dO ring and every per-step barrier run on one
 // step counter across items, so the next item's first loads and MMAs start
 // while this item's last dQ tile drains and its dK/dV are written out: V is
 // released after the item's last dP^T, K after its last dQ, and dK/dV go from
@@ -117,9 +117,6 @@ enum : int {
   kBarDkvEmpty = 20, // dK_j / dV_j have been read out of TMEM
 };
 
-// The m-th work item of this CTA: K/V tile j of head bh, with the Q tiles
-// i0 .. n_tiles-1.  Items are numbered heaviest first (k = j * BH + bh) and
-// dealt in snake order.  Returns false past the last item.
 // A work item: K/V tile j of head bh, walking n_it Q tiles.  Step it visits
 // Q tile qtile(it): i0 + it (causal: i0 = j), or, without a mask and without
 // the ordered dQ reduction, (j + it) mod n_tiles, so that the K/V tiles of one
@@ -138,11 +135,13 @@ __device__ __forceinline__ int qtile(const BwdItem& w, int it, int n_tiles) {
   }
 }
 
-// Items are numbered in sections of sec_heads heads (sized so that a
-// section's dQ accumulator, Q, dO, L and D stay in L2 while its items run)
+// The m-th work item of this CTA (false past the last one).  Items are
+// numbered in sections of sec_heads heads (sized so that a section's dQ
+// accumulator, Q, dO, L and D stay in L2 while its items run; one section of
+// all heads in the ordered mode and for causal runs that cannot be paired)
 // and, inside a section, heaviest first: by j (causal: K/V tile j has
-// n_tiles - j Q tiles), heads inner.  The m-th item of this CTA is dealt in
-// snake order over the CTAs.
+// n_tiles - j Q tiles), heads inner.  They are dealt in snake order over the
+// CTAs.
 //
 // Causal with paired items (a.paired: even n_tiles, any-order dQ): the CTA's
 // items 2q and 2q + 1 are K/V tiles p and n_tiles - 1 - p of one head, the
