@@ -78,9 +78,15 @@ def _heads_subset(w, count, seed):
     return torch.randperm(w.B * w.H, generator=g)[:count].tolist()
 
 
+# Non-causal, 128 heads: the items run in several L2-sized head sections and
+# every K/V tile starts its walk on a different Q tile.
+SECTIONS_NONCAUSAL = W.Workload("b8h16_n2048_d128_sections", 8, 16, 2048, 128, False, seed=1006)
+
+
 @pytest.mark.parametrize("w,q_rows,k_rows,k_heads", [
     (W.CAUSAL_OUTLIERS, 48, 32, 3),
     (W.LONG_CAUSAL, 256, 32, 1),
+    (SECTIONS_NONCAUSAL, 24, 16, 2),
 ])
 def test_bwd_full_size_sampled(w, q_rows, k_rows, k_heads):
     """Full-size launch.  dQ is checked on seeded query rows of every head;
