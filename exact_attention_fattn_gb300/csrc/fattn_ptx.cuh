@@ -56,12 +56,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-               "r"(bytes)
-               : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -123,24 +117,6 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int c0,
-                                            int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int c0, int c1,
-                                             int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(tmap)),
-      "r"(src), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
 // Element-wise add of a shared-memory box into global memory through a
 // tensor map (fp32 here): global[box] += shared[box].  Out-of-range rows of
 // the box are skipped.
@@ -168,21 +144,6 @@ __device__ __forceinline__ void bulk_wait_group_read1() {
 
 __device__ __forceinline__ void bulk_wait_group0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// Bulk (non-tensor) reduction of fp32 values from shared into global memory:
-// global[i] += shared[i] for `bytes` bytes (multiple of 16, both 16-aligned).
-__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
-  asm volatile(
-      "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
-      "r"(ssrc), "r"(bytes)
-      : "memory");
-}
-
-// global += v (fp32), no return value.
-__device__ __forceinline__ void red_add_f32(float* gaddr, uint32_t v) {
-  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(gaddr), "f"(__uint_as_float(v))
-               : "memory");
 }
 
 // Make generic-proxy shared-memory writes visible to the async proxy (TMA).
@@ -280,33 +241,12 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D(tmem) (+)= A(smem) * B(smem)
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D(tmem) (+)= A(tmem) * B(smem)
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Converged-warp forms.  The whole warp executes these (same operands in
 // every lane) and elect.sync picks the one lane that issues.  Issuing from a
 // converged warp keeps the operands on the uniform datapath; measured on
 // GB300, a 128x128x16 MMA then issues every 64 cycles (the tensor rate),
 // against ~107 cycles when one lane issues inside a divergent branch.
+// D(tmem) (+)= A(smem) * B(smem), bf16 operands; accumulate when nonzero.
 __device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -341,6 +281,7 @@ __device__ __forceinline__ void mma_ts_f8_w(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// D(tmem) (+)= A(tmem) * B(smem), bf16 operands.
 __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -410,14 +351,6 @@ __device__ __forceinline__ void bulk_load_1d_w(uint32_t dst, const void* src, ui
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& w,
                                                unsigned int site) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, w, site));
-}
-
-// Arrive once on `bar` when every tcgen05 MMA issued so far by this thread
-// has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base+i),
