@@ -61,6 +61,11 @@ def test_workspace_bytes(lib):
                                                              + al(4 * rows * d) + counters)
     assert lib.fattn_bwd_workspace_bytes(0, 1, 1, 64) == 0
     assert lib.fattn_bwd_workspace_bytes(1, 1, 1, 96) == 0
+    # the size limit: fewer than 2^31 elements per [B, H, N, d] tensor
+    assert lib.fattn_bwd_workspace_bytes(1, 1, (1 << 24) - 1, 128) > 0
+    assert lib.fattn_bwd_workspace_bytes(1, 1, 1 << 24, 128) == 0
+    assert lib.fattn_bwd_workspace_bytes(2, 4, 1 << 21, 128) == 0
+    assert lib.fattn_bwd_workspace_bytes(2, 4, (1 << 21) - 1, 128) > 0
 
 
 GOOD = 0x10000  # a 16-byte aligned fake address; never dereferenced

@@ -9,7 +9,7 @@ import oracle
 from exact_attention_fattn_gb300 import attention as A
 from exact_attention_fattn_gb300 import workloads as W
 from gpu_util import gather_rows, run_fwd, to_np
-from tolerances import check_grad
+from tolerances import check_grad, check_l, check_o
 
 pytestmark = pytest.mark.gpu
 
@@ -153,3 +153,27 @@ def test_bwd_workspace_reuse_and_stream():
     assert torch.equal(r1[1], r2[1]) and torch.equal(r1[2], r2[2])
     gq, _, _, _ = oracle.attention_backward(inp["q"], inp["k"], inp["v"], inp["do"], True, w.scale)
     check_grad(to_np(r2[0]), gq, "dQ")
+
+
+def test_long_sequence_65536():
+    """N = 65536 (512 tiles per head), causal: O, L and dQ on seeded rows of
+    both heads against the oracle; dK, dV through the identities that hold at
+    any size (the oracle's key rows would need every query row's softmax)."""
+    w = W.Workload("b1h2_n65536_d128_causal", 1, 2, 65536, 128, True, seed=1007)
+    inp = W.make_inputs(w)
+    o, lse = run_fwd(inp, True, w.scale)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    dq, dk, dv = A.fattn_bwd(q, k, v, o, do, lse, causal=True, scale=w.scale)
+    assert A.fattn_check_status() == 0
+    r = W.sample_rows(w, 24, seed=w.seed + 1)
+    o_ref, l_ref = oracle.attention_forward_rows(inp["q"], inp["k"], inp["v"], r.numpy(), True,
+                                                 w.scale)
+    check_o(gather_rows(o, r), o_ref)
+    check_l(gather_rows(lse, r), l_ref)
+    gq = oracle.attention_backward_query_rows(inp["q"], inp["k"], inp["v"], inp["do"],
+                                              r.numpy(), True, w.scale)
+    check_grad(gather_rows(dq, r), gq, "dQ")
+    dk64, dv64, do64 = to_np(dk), to_np(dv), to_np(inp["do"])
+    assert (np.abs(dk64.sum(axis=2)) <= 2.0 ** -7 * np.abs(dk64).sum(axis=2)).all()
+    assert (np.abs(dv64.sum(axis=2) - do64.sum(axis=2))
+            <= 2.0 ** -7 * np.abs(dv64).sum(axis=2) + 1e-6).all()
