@@ -33,6 +33,15 @@ def _check_inputs(tensors, d_expected=None):
             raise ValueError("tensors must be on one device")
 
 
+def _check_out(t, shape, dtype, device, name):
+    """A caller-provided output buffer must be exactly what the kernel writes."""
+    if (t.dtype != dtype or tuple(t.shape) != tuple(shape) or t.device != device
+            or not t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} "
+                         f"on {device}")
+    return t
+
+
 def default_scale(d: int) -> float:
     """1/sqrt(d) ("6.1 FlashAttention V1详解" §1.1), as an fp32 value."""
     return float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
@@ -43,8 +52,9 @@ def fattn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=Non
     _check_inputs([q, k, v])
     B, H, N, d = q.shape
     scale = default_scale(d) if scale is None else float(scale)
-    o = torch.empty_like(q) if out is None else out
-    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    o = torch.empty_like(q) if out is None else _check_out(out, q.shape, q.dtype, q.device, "out")
+    l = (torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None
+         else _check_out(lse, (B, H, N), torch.float32, q.device, "lse"))
     lib = _lib.load()
     with torch.cuda.device(q.device):
         rc = lib.fattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
@@ -67,9 +77,9 @@ def fattn_quantize_fp8(x, transposed: bool = False, signs=None):
     if signs is not None:
         if transposed:
             raise ValueError("the rotation applies to Q and K, which are not transposed")
-        if (signs.dtype != torch.float32 or not signs.is_cuda or signs.numel() != d
+        if (signs.dtype != torch.float32 or signs.device != x.device or signs.numel() != d
                 or not signs.is_contiguous()):
-            raise TypeError("signs must be a contiguous fp32 CUDA tensor of d values")
+            raise TypeError("signs must be a contiguous fp32 tensor of d values on x's device")
         if d != 128:
             raise ValueError("the FP8 path supports d = 128 only")
         codes = torch.empty((B, H, N, d), dtype=torch.uint8, device=x.device)
@@ -104,12 +114,19 @@ def fattn_fwd_fp8(q8, sq, k8, sk, v8t, sv, causal: bool = False, scale: float | 
     for t in (sq, sk, sv):
         if t.dtype != torch.float32 or not t.is_contiguous():
             raise TypeError("scales must be contiguous fp32 tensors")
+    if any(t.device != q8.device for t in (k8, v8t, sq, sk, sv)):
+        raise ValueError("codes and scales must be on one CUDA device")
     B, H, N, d = q8.shape
     if k8.shape != q8.shape or v8t.shape[:3] != (B, H, d):
         raise ValueError("q8, k8 must be [B,H,N,d] and v8t [B,H,d,Np]")
+    nt = (N + 127) // 128
+    if any(t.shape != (B, H, nt) for t in (sq, sk, sv)):
+        raise ValueError("scales must be [B,H,ceil(N/128)] fp32 (one per 128-row block)")
     scale = default_scale(d) if scale is None else float(scale)
-    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
-    l = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    o = (torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if out is None
+         else _check_out(out, (B, H, N, d), torch.bfloat16, q8.device, "out"))
+    l = (torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None
+         else _check_out(lse, (B, H, N), torch.float32, q8.device, "lse"))
     lib = _lib.load()
     with torch.cuda.device(q8.device):
         rc = lib.fattn_fwd_fp8(q8.data_ptr(), sq.data_ptr(), k8.data_ptr(), sk.data_ptr(),
@@ -132,18 +149,23 @@ def workspace_for(q) -> torch.Tensor:
     return torch.empty(nbytes, dtype=torch.uint8, device=q.device)
 
 
+def _check_workspace(ws, q):
+    if ws.dtype != torch.uint8 or ws.device != q.device or not ws.is_contiguous():
+        raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
+    return ws   # its size is checked by the library
+
+
 def fattn_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
               workspace=None, dq=None, dk=None, dv=None):
     """Backward pass; returns (dQ, dK, dV), bf16 [B,H,N,d]."""
     _check_inputs([q, k, v, o, do])
     B, H, N, d = q.shape
-    if lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    _check_out(lse, (B, H, N), torch.float32, q.device, "lse")
     scale = default_scale(d) if scale is None else float(scale)
-    ws = workspace_for(q) if workspace is None else workspace
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    ws = workspace_for(q) if workspace is None else _check_workspace(workspace, q)
+    dq = torch.empty_like(q) if dq is None else _check_out(dq, q.shape, q.dtype, q.device, "dq")
+    dk = torch.empty_like(k) if dk is None else _check_out(dk, q.shape, q.dtype, q.device, "dk")
+    dv = torch.empty_like(v) if dv is None else _check_out(dv, q.shape, q.dtype, q.device, "dv")
     lib = _lib.load()
     with torch.cuda.device(q.device):
         rc = lib.fattn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
@@ -157,6 +179,8 @@ def fattn_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None = N
 def fattn_bwd_prepare(o, do, lse, workspace):
     _check_inputs([o, do])
     B, H, N, d = o.shape
+    _check_out(lse, (B, H, N), torch.float32, o.device, "lse")
+    _check_workspace(workspace, o)
     lib = _lib.load()
     with torch.cuda.device(o.device):
         rc = lib.fattn_bwd_prepare(o.data_ptr(), do.data_ptr(), lse.data_ptr(),
@@ -168,6 +192,7 @@ def fattn_bwd_prepare(o, do, lse, workspace):
 def fattn_bwd_main(q, k, v, do, workspace, dk, dv, causal: bool = False,
                    scale: float | None = None):
     _check_inputs([q, k, v, do, dk, dv])
+    _check_workspace(workspace, q)
     B, H, N, d = q.shape
     scale = default_scale(d) if scale is None else float(scale)
     lib = _lib.load()
@@ -180,6 +205,8 @@ def fattn_bwd_main(q, k, v, do, workspace, dk, dv, causal: bool = False,
 
 
 def fattn_bwd_finish(workspace, dq, scale: float | None = None):
+    _check_inputs([dq])
+    _check_workspace(workspace, dq)
     B, H, N, d = dq.shape
     scale = default_scale(d) if scale is None else float(scale)
     lib = _lib.load()
@@ -192,6 +219,8 @@ def fattn_bwd_finish(workspace, dq, scale: float | None = None):
 def fattn_bwd_preprocess(o, do, D, dq_accum):
     _check_inputs([o, do])
     B, H, N, d = o.shape
+    _check_out(D, (B, H, N), torch.float32, o.device, "D")
+    _check_out(dq_accum, (B, H, N, d), torch.float32, o.device, "dq_accum")
     lib = _lib.load()
     with torch.cuda.device(o.device):
         rc = lib.fattn_bwd_preprocess(o.data_ptr(), do.data_ptr(), D.data_ptr(),
