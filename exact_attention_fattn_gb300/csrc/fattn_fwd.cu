@@ -252,13 +252,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kv0 = j * kBN;
         const bool need_mask = (kv0 + kBN > N) || (CAUSAL && kv0 + kBN - 1 > qs);
         if (need_mask) {
+          // columns kv0 + c with c < lim are visible: c < N - kv0 and, causal,
+          // kv0 + c <= row
+          const int lim = (CAUSAL ? min(N, row + 1) : N) - kv0;
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int col = kv0 + g * 32 + i;
-              if (col >= N || (CAUSAL && col > row)) sv[g][i] = __float_as_uint(-INFINITY);
-            }
+            for (int i = 0; i < 32; ++i)
+              if (g * 32 + i >= lim) sv[g][i] = __float_as_uint(-INFINITY);
           }
         }
         // Row max as four independent 3-input max chains (one per 32-column
