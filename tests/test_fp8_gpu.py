@@ -170,3 +170,27 @@ def test_rotated_quantize_rejects_transposed_and_d64():
     x64 = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(ValueError):
         A.fattn_quantize_fp8(x64, signs=torch.ones(64, dtype=torch.float32, device="cuda"))
+
+
+def test_fwd_fp8_tiny_value_block():
+    """One V block about 1e-35 of the others: its block-scale ratio rho is far
+    below 2^-100, where the forward clamps log2(rho).  The output stays finite
+    and matches the exact attention of the dequantized inputs within the FP8
+    bound (that block's contribution rounds to e4m3 zero either way), and L
+    is unaffected (the row sums still count its probabilities)."""
+    w = W.Workload("f8tiny", 1, 2, 512, 128, False, backward=False, seed=991)
+    inp = W.make_inputs(w)
+    inp["v"][:, :, 128:256] = (inp["v"][:, :, 128:256].float() * 1e-35).to(torch.bfloat16)
+    q8, sq, k8, sk, v8t, sv = _quantize_all(inp)
+    assert float(sv[0, 0, 1]) / float(sv.max()) < 2.0 ** -100
+    o, lse = A.fattn_fwd_fp8(q8, sq, k8, sk, v8t, sv, causal=False, scale=w.scale)
+    assert A.fattn_check_status() == 0
+    o_np, l_np = to_np(o), to_np(lse)
+    assert np.isfinite(o_np).all() and np.isfinite(l_np).all()
+    o_ref, l_ref = oracle.attention_fp8_reference(q8.cpu().numpy(), sq.cpu().numpy(),
+                                                  k8.cpu().numpy(), sk.cpu().numpy(),
+                                                  v8t.cpu().numpy(), sv.cpu().numpy(),
+                                                  False, w.scale)
+    v_deq = oracle.block_dequantize(v8t.cpu().numpy(), sv.cpu().numpy(), w.N, transposed=True)
+    check_o_fp8(o_np, o_ref, float(np.abs(v_deq).max()))
+    check_l(l_np, l_ref)
