@@ -81,12 +81,19 @@ def _heads_subset(w, count, seed):
 # Non-causal, 128 heads: the items run in several L2-sized head sections and
 # every K/V tile starts its walk on a different Q tile.
 SECTIONS_NONCAUSAL = W.Workload("b8h16_n2048_d128_sections", 8, 16, 2048, 128, False, seed=1006)
+# The same with a ragged last tile (16 tiles, the last 80 rows long).
+SECTIONS_RAGGED = W.Workload("b8h16_n2000_d128_sections", 8, 16, 2000, 128, False, seed=1008)
+# Causal with an odd number of tiles: the items keep the all-heads order
+# (no pairing); 64 heads, so several items of a head run at once.
+CAUSAL_ODD_TILES = W.Workload("b4h16_n1920_d128_causal", 4, 16, 1920, 128, True, seed=1009)
 
 
 @pytest.mark.parametrize("w,q_rows,k_rows,k_heads", [
     (W.CAUSAL_OUTLIERS, 48, 32, 3),
     (W.LONG_CAUSAL, 256, 32, 1),
     (SECTIONS_NONCAUSAL, 24, 16, 2),
+    (SECTIONS_RAGGED, 24, 16, 2),
+    (CAUSAL_ODD_TILES, 24, 16, 2),
 ])
 def test_bwd_full_size_sampled(w, q_rows, k_rows, k_heads):
     """Full-size launch.  dQ is checked on seeded query rows of every head;
