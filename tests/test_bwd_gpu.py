@@ -86,6 +86,8 @@ SECTIONS_RAGGED = W.Workload("b8h16_n2000_d128_sections", 8, 16, 2000, 128, Fals
 # Causal with an odd number of tiles: the items keep the all-heads order
 # (no pairing); 64 heads, so several items of a head run at once.
 CAUSAL_ODD_TILES = W.Workload("b4h16_n1920_d128_causal", 4, 16, 1920, 128, True, seed=1009)
+# d = 64 with several head sections (256 heads).
+SECTIONS_D64 = W.Workload("b8h32_n4096_d64_sections", 8, 32, 4096, 64, False, seed=1010)
 
 
 @pytest.mark.parametrize("w,q_rows,k_rows,k_heads", [
@@ -94,6 +96,7 @@ CAUSAL_ODD_TILES = W.Workload("b4h16_n1920_d128_causal", 4, 16, 1920, 128, True,
     (SECTIONS_NONCAUSAL, 24, 16, 2),
     (SECTIONS_RAGGED, 24, 16, 2),
     (CAUSAL_ODD_TILES, 24, 16, 2),
+    (SECTIONS_D64, 8, 16, 2),
 ])
 def test_bwd_full_size_sampled(w, q_rows, k_rows, k_heads):
     """Full-size launch.  dQ is checked on seeded query rows of every head;

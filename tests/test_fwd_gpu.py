@@ -76,7 +76,9 @@ def test_fwd_medium_d64_full():
 
 
 @pytest.mark.parametrize("w,rows", [(W.CAUSAL_OUTLIERS, 48), (W.LONG_CAUSAL, 256)]
-                         + [(W.SWEEP_D128.with_n(n), 48) for n in W.SWEEP_NS])
+                         + [(W.SWEEP_D128.with_n(n), 48) for n in W.SWEEP_NS]
+                         + [(W.Workload("b8h32_n4096_d64_sections", 8, 32, 4096, 64, False,
+                                        backward=False, seed=1010), 8)])
 def test_fwd_full_size_sampled_rows(w, rows):
     """Full-size launch; the oracle evaluates a seeded sample of rows per head
     (always including the first and the last row)."""
