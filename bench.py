@@ -37,10 +37,12 @@ sys.path.insert(0, ROOT)
 METRIC = "attention fwd/bwd TFLOP/s and fraction of GB300 dense BF16 peak"
 DEFAULT_WORKLOAD = "b2h32_n4096_d128_causal_outliers"
 KERNEL_SOURCES = {
-    "fwd": "exact_attention_fattn_gb300/csrc/fattn_fwd.cu",
-    "bwd_main": "exact_attention_fattn_gb300/csrc/fattn_bwd.cu",
-    "bwd_prepare": "exact_attention_fattn_gb300/csrc/fattn_bwd_aux.cu",
-    "bwd_finish": "exact_attention_fattn_gb300/csrc/fattn_bwd_aux.cu",
+    "fwd": ("exact_attention_fattn_gb300/csrc/fattn_fwd.cu",),
+    "bwd_main": ("exact_attention_fattn_gb300/csrc/fattn_bwd.cu",
+                 "exact_attention_fattn_gb300/csrc/fattn_sched.h",
+                 "exact_attention_fattn_gb300/csrc/fattn_sched.cu"),
+    "bwd_prepare": ("exact_attention_fattn_gb300/csrc/fattn_bwd_aux.cu",),
+    "bwd_finish": ("exact_attention_fattn_gb300/csrc/fattn_bwd_aux.cu",),
 }
 L2_BYTES = 129 * 10**6
 
@@ -61,11 +63,14 @@ def load_peaks():
         return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
 
 
-def source_hash(rel):
-    """sha256[:16] of a kernel source with its comments and whitespace
-    removed, so that only a change to the code invalidates a capture."""
-    with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
-        src = f.read()
+def source_hash(rels):
+    """sha256[:16] of a kernel's source files, concatenated, with comments and
+    whitespace removed, so that only a change to the code (the kernel or the
+    schedule it runs) invalidates a capture."""
+    src = ""
+    for rel in rels:
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            src += f.read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     src = re.sub(r"//[^\n]*", "", src)
     src = re.sub(r"\s+", "", src)

@@ -228,6 +228,24 @@ def fattn_bwd_preprocess(o, do, D, dq_accum):
     _lib.check("fattn_bwd_preprocess", rc)
 
 
+def fattn_bwd_schedule(B: int, H: int, N: int, d: int, causal: bool, grid: int, l2_bytes: int,
+                       deterministic: bool = False):
+    """The backward kernel's static work schedule, computed on the host.
+
+    Returns (item_cta, cta_q_tiles): int32 [B*H, ceil(N/128)] with the CTA
+    that processes each K/V tile (-1 none, -2 several), and int64 [grid] with
+    the Q tiles each CTA walks.  Needs no GPU.
+    """
+    n_tiles = (N + 127) // 128
+    item_cta = torch.empty(B * H * n_tiles, dtype=torch.int32)
+    cta_q_tiles = torch.empty(max(grid, 0), dtype=torch.int64)
+    rc = _lib.load().fattn_bwd_schedule(B, H, N, d, int(bool(causal)), int(bool(deterministic)),
+                                        grid, l2_bytes, item_cta.data_ptr(),
+                                        cta_q_tiles.data_ptr())
+    _lib.check("fattn_bwd_schedule", rc)
+    return item_cta.view(B * H, n_tiles), cta_q_tiles
+
+
 def fattn_check_status(device=None) -> int:
     """Synchronise the current stream and return (and clear) the status."""
     dev = torch.device("cuda") if device is None else torch.device(device)

@@ -9,6 +9,7 @@
 #include "../../include/fattn.h"
 #include "fattn_internal.h"
 #include "fattn_ptx.cuh"
+#include "fattn_sched.h"
 
 namespace fattn {
 
@@ -415,6 +416,36 @@ int fattn_bwd(const void* q, const void* k, const void* v, const void* o, const 
                           st)) != FATTN_OK)
     return rc;
   return bwd_finish_impl(workspace, dq, B, H, N, d, scale, st);
+}
+
+int fattn_bwd_schedule(int B, int H, int N, int d, int causal, int deterministic, int grid,
+                       long long l2_bytes, int* item_cta, long long* cta_q_tiles) {
+  const int rc = check_sizes(B, H, N, d);
+  if (rc != FATTN_OK) return rc;
+  if (grid <= 0 || l2_bytes < 0 || !item_cta) return FATTN_ERR_INVALID_ARG;
+  const int BH = B * H;
+  const int n_tiles = (N + 127) / 128;
+  const long long items = static_cast<long long>(n_tiles) * BH;
+  if (items > (1ll << 24) || grid > items) return FATTN_ERR_INVALID_ARG;
+  BwdArgs a{};
+  a.N = N;
+  a.BH = BH;
+  plan_bwd_schedule(a, n_tiles, d, causal != 0, deterministic != 0, grid, l2_bytes);
+  for (long long i = 0; i < items; ++i) item_cta[i] = -1;
+  for (int c = 0; c < grid; ++c) {
+    long long walked = 0;
+    BwdItem w;
+    for (int m = 0; m <= items; ++m) {
+      const bool more = causal ? bwd_item<true>(m, n_tiles, a, grid, c, w)
+                               : bwd_item<false>(m, n_tiles, a, grid, c, w);
+      if (!more) break;
+      int& slot = item_cta[static_cast<long long>(w.bh) * n_tiles + w.j];
+      slot = slot == -1 ? c : -2;
+      walked += w.n_it;
+    }
+    if (cta_q_tiles) cta_q_tiles[c] = walked;
+  }
+  return FATTN_OK;
 }
 
 int fattn_check_status(fattn_stream_t stream) {

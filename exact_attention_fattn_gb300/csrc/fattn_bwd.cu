@@ -45,6 +45,7 @@
 // computed into A while the dQ rows are being read out.
 #include "fattn_internal.h"
 #include "fattn_ptx.cuh"
+#include "fattn_sched.h"
 
 namespace fattn {
 
@@ -127,14 +128,7 @@ __device__ __forceinline__ int dq_empty(uint32_t step) {
   return (step & 1) ? kBarDqEmpty1 : kBarDqEmpty;
 }
 
-// A work item: K/V tile j of head bh, walking n_it Q tiles.  Step it visits
-// Q tile qtile(it): i0 + it (causal: i0 = j), or, without a mask and without
-// the ordered dQ reduction, (j + it) mod n_tiles, so that the K/V tiles of one
-// head start on different Q tiles instead of all reduce-adding into tile 0.
-struct BwdItem {
-  int j, bh, i0, n_it, rot;
-};
-
+// The Q tile that step it of item w visits (see BwdItem).
 template <bool CAUSAL>
 __device__ __forceinline__ int qtile(const BwdItem& w, int it, int n_tiles) {
   if constexpr (CAUSAL) {
@@ -145,62 +139,19 @@ __device__ __forceinline__ int qtile(const BwdItem& w, int it, int n_tiles) {
   }
 }
 
-// The m-th work item of this CTA (false past the last one).  Items are
-// numbered in sections of sec_heads heads (sized so that a section's dQ
-// accumulator, Q, dO, L and D stay in L2 while its items run; one section of
-// all heads in the ordered mode and for causal runs that cannot be paired)
-// and, inside a section, heaviest first: by j (causal: K/V tile j has
-// n_tiles - j Q tiles), heads inner.  They are dealt in snake order over the
-// CTAs.
-//
-// Causal with paired items (a.paired: even n_tiles, any-order dQ): the CTA's
-// items 2q and 2q + 1 are K/V tiles p and n_tiles - 1 - p of one head, the
-// q-th pair dealt to it, so every pair walks n_tiles + 1 Q tiles and the pairs
-// can be numbered in head sections without unbalancing the CTAs.
+// The m-th work item of this CTA (false past the last one); see bwd_item.
 template <bool CAUSAL>
 __device__ __forceinline__ bool get_bwd_item(int m, int n_tiles, const BwdArgs& a, BwdItem& w) {
-  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-  if (CAUSAL && a.paired) {
-    const int n_pairs = n_tiles >> 1;
-    const int q = m >> 1;
-    const long long k = static_cast<long long>(q) * G + ((q & 1) ? (G - 1 - c) : c);
-    if (k >= static_cast<long long>(n_pairs) * a.BH) return false;
-    const int kk = static_cast<int>(k);
-    const int sec_items = a.sec_heads * n_pairs;
-    const int sec = kk / sec_items;
-    const int kp = kk - sec * sec_items;
-    const int h0 = sec * a.sec_heads;
-    const int hs = min(a.sec_heads, a.BH - h0);
-    const int p = kp / hs;
-    w.bh = h0 + kp % hs;
-    w.j = (m & 1) ? n_tiles - 1 - p : p;
-    w.i0 = w.j;
-    w.n_it = n_tiles - w.i0;
-    w.rot = 0;
-    return true;
-  }
-  const long long k = static_cast<long long>(m) * G + ((m & 1) ? (G - 1 - c) : c);
-  if (k >= static_cast<long long>(n_tiles) * a.BH) return false;
-  // item counts fit in int (the launcher checks n_tiles * BH < 2^31)
-  const int kk = static_cast<int>(k);
-  const int sec_items = a.sec_heads * n_tiles;
-  const int sec = kk / sec_items;
-  const int kp = kk - sec * sec_items;
-  const int h0 = sec * a.sec_heads;
-  const int hs = min(a.sec_heads, a.BH - h0);
-  w.j = kp / hs;
-  w.bh = h0 + kp % hs;
-  w.i0 = CAUSAL ? w.j : 0;
-  w.n_it = n_tiles - w.i0;
-  w.rot = (!CAUSAL && a.dq_order == nullptr) ? w.j : 0;
-  return true;
+  return bwd_item<CAUSAL>(m, n_tiles, a, static_cast<int>(gridDim.x),
+                          static_cast<int>(blockIdx.x), w);
 }
 
 template <int HD, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-               const __grid_constant__ CUtensorMap tm_dqacc, const BwdArgs args) {
+               const __grid_constant__ CUtensorMap tm_dqacc,
+               const __grid_constant__ BwdArgs args) {
   using C = BwdCfg<HD>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -763,21 +714,8 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   const long long items = static_cast<long long>(n_tiles) * a.BH;
   if (items >= 0x7fffffffLL) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(items < sms ? items : sms));
-  // Heads per section: a third of L2 over what one head's steps keep
-  // re-reading (fp32 dQ accumulator, Q, dO, L, D).  Not with the ordered
-  // reduction: there the items of a head wait on each other at every Q tile,
-  // and the more of them run at once the longer the chains (measured on
-  // GB300: 1.8x slower).  Causal items are paired first (equal weights), or
-  // keep the all-heads heaviest-first order when n_tiles is odd.
   BwdArgs ab = a;
-  ab.sec_heads = a.BH;
-  ab.paired = CAUSAL && a.dq_order == nullptr && (n_tiles % 2) == 0 ? 1 : 0;
-  if ((!CAUSAL || ab.paired) && a.dq_order == nullptr) {
-    const long long per_head =
-        static_cast<long long>(n_tiles) * kTile * (HD * 4 + 2 * HD * 2 + 2 * 4);
-    const long long fit = per_head > 0 ? (static_cast<long long>(l2) / 3) / per_head : 1;
-    ab.sec_heads = static_cast<int>(fit < 1 ? 1 : (fit > a.BH ? a.BH : fit));
-  }
+  plan_bwd_schedule(ab, n_tiles, HD, CAUSAL, a.dq_order != nullptr, static_cast<int>(grid.x), l2);
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tacc, ab);
   return cudaGetLastError();
 }

@@ -49,6 +49,10 @@ cudaError_t launch_fp8_quantize_rotated(const void* x, const float* signs, void*
                                         float* scales, int BH, int N, int d,
                                         cudaStream_t stream);
 
+// Capacity of the backward's tail tables (kernel parameters, ~2.6 KB).
+constexpr int kBwdTailMaxCtas = 256;
+constexpr int kBwdTailCap = 1024;
+
 struct BwdArgs {
   const float* L2;            // [BH, Np]: -lse * log2(e), -inf past N (Np = N rounded up to 128)
   const float* D;             // [BH, Np]: rowsum(dO o O), 0 past N
@@ -64,6 +68,11 @@ struct BwdArgs {
   int paired;                 // causal K/V tiles p and n - 1 - p paired (set by the launcher)
   float scale;
   float scale_log2;
+  // Paired causal schedule only (set by the launcher, see bwd_item): the
+  // last tail_heads heads are dealt K/V tile by K/V tile from these tables.
+  int tail_heads;
+  uint16_t tail_off[kBwdTailMaxCtas + 1];  // CTA c: entries [tail_off[c], tail_off[c + 1])
+  uint16_t tail_item[kBwdTailCap];         // r * n_tiles + j: K/V tile j of head BH - tail_heads + r
 };
 
 // D (and, when L2 != nullptr, L2 = -lse * log2 e) in a [BH, pitch] layout with

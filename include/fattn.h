@@ -211,6 +211,30 @@ int fattn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o
                       fattn_stream_t stream);
 
 /*
+ * The static work schedule of the backward's main kernel, computed on the
+ * host (no GPU, no CUDA call, nothing enqueued).  A work item is the 128-row
+ * K/V tile j of head bh = b*H + h, which walks its Q tiles (causal: tiles
+ * j..n_tiles-1; n_tiles = ceil(N/128)); the kernel runs one CTA per SM, each
+ * working through a list of items fixed before the launch ("FlashAttention
+ * v1～v4" v4 §4: persistent scheduling, heaviest first, L2-aware head order).
+ *   B, H, N, d    : as for fattn_bwd_main; causal, deterministic as there
+ *                   (deterministic = the mode of fattn_set_deterministic)
+ *   grid          : number of CTAs; a launch uses min(SM count, B*H*n_tiles)
+ *   l2_bytes      : L2 size the head sections are sized for
+ *                   (cudaDevAttrL2CacheSize on the device)
+ *   item_cta      : out, int [B*H*n_tiles], caller-owned host memory: at
+ *                   [bh*n_tiles + j] the CTA that processes K/V tile j of head
+ *                   bh; -1 if no CTA does, -2 if several do (neither happens)
+ *   cta_q_tiles   : out, optional (NULL), long long [grid], host memory: the
+ *                   Q tiles each CTA walks, i.e. its share of the work
+ * Returns FATTN_ERR_INVALID_ARG for bad sizes, grid < 1, grid above the item
+ * count, more than 2^24 items or a NULL item_cta; FATTN_ERR_UNSUPPORTED for
+ * d not in {64, 128}.
+ */
+int fattn_bwd_schedule(int B, int H, int N, int d, int causal, int deterministic, int grid,
+                       long long l2_bytes, int* item_cta, long long* cta_q_tiles);
+
+/*
  * Synchronise `stream`, then report the first error since the last call:
  * a pending asynchronous CUDA error (FATTN_ERR_CUDA) or a kernel wait
  * timeout recorded on the current device (FATTN_ERR_TIMEOUT).  Clears the

@@ -1,0 +1,111 @@
+"""The backward kernel's static work schedule, read through the C ABI on the
+host (no GPU): the very mapping the kernel runs (its item function is
+compiled for both sides) gives every K/V tile of every head to exactly one
+CTA, and balances the CTAs' shares of the Q-tile walk."""
+
+import ctypes
+import math
+import os
+
+import pytest
+
+from exact_attention_fattn_gb300 import _lib
+from exact_attention_fattn_gb300.attention import fattn_bwd_schedule
+
+L2 = 126 * 2**20  # an L2 of GB300's size (the head sections are sized from it)
+SMS = 152
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not os.path.exists(_lib.LIB_PATH):
+        from exact_attention_fattn_gb300 import build
+
+        build.build()
+    return _lib.load()
+
+
+def walk(n_tiles, causal):
+    """Q tiles that K/V tile j walks (causal: j..n_tiles-1)."""
+    return [n_tiles - j if causal else n_tiles for j in range(n_tiles)]
+
+
+def grid_for(B, H, N):
+    return min(SMS, B * H * math.ceil(N / 128))
+
+
+CASES = [
+    # B, H, N, d, causal, deterministic
+    (2, 32, 4096, 128, True, False),    # causal bench shape: paired + tail
+    (1, 16, 16384, 128, True, False),   # long causal
+    (1, 2, 65536, 64, True, False),     # few heads, long walks
+    (8, 16, 4096, 128, False, False),   # unmasked, head sections
+    (2, 32, 4096, 128, True, True),     # ordered dQ: one section, unpaired
+    (1, 3, 1920, 128, True, False),     # odd tile count: unpaired causal
+    (1, 1, 128, 64, True, False),       # one item
+    (3, 5, 2000, 64, True, False),      # ragged N, small grid
+    (4, 8, 1024, 128, False, True),
+    (16, 16, 1024, 128, True, False),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,det", CASES)
+def test_every_item_exactly_once(B, H, N, d, causal, det):
+    grid = grid_for(B, H, N)
+    item_cta, q_tiles = fattn_bwd_schedule(B, H, N, d, causal, grid, L2, deterministic=det)
+    assert item_cta.min().item() >= 0, "a K/V tile is missing or scheduled twice"
+    assert item_cta.max().item() < grid
+    n_tiles = math.ceil(N / 128)
+    total = B * H * sum(walk(n_tiles, causal))
+    assert q_tiles.sum().item() == total
+    # the CTA's share is the sum of its items' walks
+    per_cta = [0] * grid
+    for bh in range(B * H):
+        for j in range(n_tiles):
+            per_cta[item_cta[bh, j].item()] += walk(n_tiles, causal)[j]
+    assert per_cta == q_tiles.tolist()
+
+
+def pairs_only_makespan(BH, n_tiles, grid):
+    n_pairs = n_tiles // 2 * BH
+    return -(-n_pairs // grid) * (n_tiles + 1)
+
+
+@pytest.mark.parametrize("B,H,N,expect_max", [
+    # (bound) the most loaded CTA walks at most this many Q tiles
+    (2, 32, 4096, 224),     # 33792 Q tiles over 152 CTAs: 222.3 on average; whole pairs give 231
+    (1, 16, 16384, 880),    # average 869.1; whole pairs 903
+    (1, 4, 32768, 890),     # average 865.7; whole pairs 1028
+    (2, 16, 4096, 114),     # average 111.2; whole pairs 132
+])
+def test_causal_tail_balances(B, H, N, expect_max):
+    grid = grid_for(B, H, N)
+    _, q_tiles = fattn_bwd_schedule(B, H, N, 128, True, grid, L2)
+    n_tiles = N // 128
+    assert q_tiles.max().item() <= expect_max
+    assert q_tiles.max().item() < pairs_only_makespan(B * H, n_tiles, grid)
+    assert q_tiles.sum().item() == B * H * n_tiles * (n_tiles + 1) // 2
+
+
+@pytest.mark.parametrize("B,H,N,d", [(2, 32, 4096, 128), (4, 8, 1024, 64), (1, 12, 2048, 128)])
+def test_causal_never_worse_than_pairs(B, H, N, d):
+    grid = grid_for(B, H, N)
+    _, q_tiles = fattn_bwd_schedule(B, H, N, d, True, grid, L2)
+    assert q_tiles.max().item() <= pairs_only_makespan(B * H, N // 128, grid)
+
+
+def test_unmasked_shares_differ_by_at_most_one_item():
+    B, H, N = 8, 16, 4096
+    _, q_tiles = fattn_bwd_schedule(B, H, N, 128, False, SMS, L2)
+    assert q_tiles.max().item() - q_tiles.min().item() <= N // 128
+
+
+def test_schedule_rejects_bad_arguments():
+    lib = _lib.load()
+    buf = (ctypes.c_int * 64)()
+    assert lib.fattn_bwd_schedule(1, 1, 128, 128, 1, 0, 0, L2, buf, None) == _lib.FATTN_ERR_INVALID_ARG
+    assert lib.fattn_bwd_schedule(1, 1, 128, 128, 1, 0, 2, L2, buf, None) == _lib.FATTN_ERR_INVALID_ARG
+    assert lib.fattn_bwd_schedule(1, 1, 128, 128, 1, 0, 1, L2, None, None) == _lib.FATTN_ERR_INVALID_ARG
+    assert lib.fattn_bwd_schedule(1, 1, 128, 96, 1, 0, 1, L2, buf, None) == _lib.FATTN_ERR_UNSUPPORTED
+    assert lib.fattn_bwd_schedule(1, 1, 128, 128, 1, 0, 1, L2, buf, None) == _lib.FATTN_OK
+    assert buf[0] == 0
