@@ -15,7 +15,8 @@
 //
 // Persistent ("FlashAttention v1～v4" v4 §4 scheduling): one CTA per SM walks
 // items numbered heaviest first (causal: small j has the most Q tiles) in
-// L2-sized head sections and dealt in snake order (see get_bwd_item).  The Q/dO ring and every per-step barrier run on one
+// L2-sized head sections and dealt in snake order (see bwd_item in
+// fattn_sched.h).  The Q/dO ring and every per-step barrier run on one
 // step counter across items, so the next item's first loads and MMAs start
 // while this item's last dQ tile drains and its dK/dV are written out: V is
 // released after the item's last dP^T, K after its last dQ, and dK/dV go from
