@@ -365,38 +365,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(b.p_full[t]);
       }
       if (!ok) break;
-      // ---- epilogue: O / l_bf -> bf16 straight to global (each thread its
-      // own row), L = (m + log2 l) ln 2.  O_t's TMEM is handed back to the
-      // MMA warp as soon as it has been read.
+      // ---- epilogue: O / l_bf -> bf16 to global, L = (m + log2 l) ln 2.  O_t
+      // is read out of TMEM whole (each thread its own row) and handed back
+      // to the MMA warp before the stores.
       ok = __all_sync(0xffffffffu, mbar_wait(b.o_full[t], o_count & 1, wc, kWaitOFull));
       if (!ok) break;
       ++o_count;
       tc_fence_after();
       const float inv = sv_max / (l + l_fix);   // sv_max = 1 unless FP8
       const bool row_ok = row < N;
-      uint4* orow = reinterpret_cast<uint4*>(args.o + (static_cast<size_t>(w.bh) * N +
-                                                       (row_ok ? row : 0)) * HD);
-#pragma unroll 1
+      uint32_t pw[HD / 2];   // the row as bf16 pairs; 16-byte chunk c = words 4c .. 4c + 3
+#pragma unroll
       for (int ch = 0; ch < HD / 32; ++ch) {
         uint32_t o[32];
         tmem_ld32(tO + 32 * ch, o);
         tmem_ld_wait32(o);
         const uint64_t i2 = splat2(inv);
-        uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           uint32_t y0, y1;
           unpack2(fmul2(pack2(o[2 * i], o[2 * i + 1]), i2), y0, y1);
-          pk[i] = pack_bf16x2(__uint_as_float(y0), __uint_as_float(y1));
-        }
-        if (row_ok) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            orow[ch * 4 + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          pw[16 * ch + i] = pack_bf16x2(__uint_as_float(y0), __uint_as_float(y1));
         }
       }
       tc_fence_before();
       mbar_arrive(b.o_empty[t]);
+      // Stores of whole 128-byte lines.  Row-per-thread stores would put 32
+      // lines into every warp store, 16 bytes each, and the L1 traffic they
+      // cause slows the MMAs' shared-memory operand reads (measured on GB300:
+      // 5-10 % of the kernel).  So the 8 lanes of each group first exchange
+      // 16-byte chunks, an 8 x 8 transpose per 128-byte half row in three
+      // XOR-shuffle stages: afterwards lane i of group g holds, in chunk slot
+      // 8h + j, chunk 8h + i of the group's row j, and one warp store writes
+      // 8 lanes x 16 bytes of one row for each of the four groups.
+      const int li = lane & 7;
+#pragma unroll
+      for (int h = 0; h < HD / 64; ++h) {
+#pragma unroll
+        for (int dd = 4; dd >= 1; dd >>= 1) {
+          const bool up = (li & dd) != 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (j & dd) continue;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t lo = pw[4 * (8 * h + j) + q];
+              const uint32_t hi = pw[4 * (8 * h + j + dd) + q];
+              const uint32_t got = __shfl_xor_sync(0xffffffffu, up ? lo : hi, dd);
+              pw[4 * (8 * h + j) + q] = up ? got : lo;
+              pw[4 * (8 * h + j + dd) + q] = up ? hi : got;
+            }
+          }
+        }
+      }
+      const int grow0 = qs + wq * 32 + (lane & ~7);   // the group's row 0
+#pragma unroll
+      for (int h = 0; h < HD / 64; ++h) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (grow0 + j < N) {
+            uint4* dst = reinterpret_cast<uint4*>(
+                             args.o + (static_cast<size_t>(w.bh) * N + grow0 + j) * HD) +
+                         8 * h + li;
+            *dst = make_uint4(pw[4 * (8 * h + j)], pw[4 * (8 * h + j) + 1],
+                              pw[4 * (8 * h + j) + 2], pw[4 * (8 * h + j) + 3]);
+          }
+        }
+      }
       if (row_ok) args.lse[static_cast<size_t>(w.bh) * N + row] = (m_ref + log2f(l)) * kLn2;
     }
   } else if (warp == kMmaWarp) {
