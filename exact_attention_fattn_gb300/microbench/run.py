@@ -1,9 +1,9 @@
 """Build and run the GB300 microbenchmarks behind the kernel design choices.
 
-    python -m exact_attention_fattn_gb300.microbench.run [mma|reduce|exp2|fit ...]
+    python -m exact_attention_fattn_gb300.microbench.run [mma|reduce|exp2|load|fit ...]
 
-`mma`, `reduce` and `exp2` compile the matching .cu file for sm_103a into
-_build/ next to this file and run it on the current GPU; `fit` (CPU only)
+`mma`, `reduce`, `exp2` and `load` compile the matching .cu file for sm_103a
+into _build/ next to this file and run it on the current GPU; `fit` (CPU only)
 prints the cubic for 2^f on [-1/2, 1/2] whose coefficients exp2_rate.cu uses.
 """
 
@@ -16,7 +16,10 @@ import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 BUILD = os.path.join(HERE, "_build")
-PROGRAMS = {"mma": "mma_rate.cu", "reduce": "reduce_rate.cu", "exp2": "exp2_rate.cu"}
+PROGRAMS = {"mma": "mma_rate.cu", "reduce": "reduce_rate.cu", "exp2": "exp2_rate.cu",
+            "load": "load_rate.cu"}
+# extra link flags (load_rate.cu encodes tensor maps through the driver API)
+LINK = {"load": ["-lcuda"]}
 
 
 def fit_exp2_cubic(iters: int = 200):
@@ -47,13 +50,13 @@ def build(name: str) -> str:
     src = os.path.join(HERE, PROGRAMS[name])
     exe = os.path.join(BUILD, name + "_rate")
     cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
-           "--expt-relaxed-constexpr", src, "-o", exe]
+           "--expt-relaxed-constexpr", src, "-o", exe] + LINK.get(name, [])
     subprocess.run(cmd, check=True)
     return exe
 
 
 def main(argv: list[str]) -> int:
-    names = argv or ["fit", "mma", "reduce", "exp2"]
+    names = argv or ["fit", "mma", "reduce", "exp2", "load"]
     for name in names:
         print(f"== {name}", flush=True)
         if name == "fit":
