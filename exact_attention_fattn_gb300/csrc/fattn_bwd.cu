@@ -170,7 +170,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int N = args.N;
   const int n_tiles = (N + kTile - 1) / kTile;
   const int pitch = n_tiles * kTile;
-  const int BH = args.BH;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarKFull), 1);
