@@ -83,16 +83,28 @@ struct FwdBars {
       mma_done;
 };
 
+// A work item: the Q-tile pair starting at row q0 of head bh; tile t sees
+// n[t] key tiles (0 when it starts past N), nt = max(n[0], n[1]).
+struct Item {
+  int q0, bh, n[2], nt;
+};
+
+// First query row of tile t of an item.  With the causal mask the upper Q
+// tile of the pair has one key tile more and finishes last; it is tile 0,
+// whose MMAs each key-tile step issues first, so that at an item boundary
+// the next S of the tile that sets the pace is issued first (measured on
+// GB300: 1.3 % faster on B = 2, H = 32, N = 4096, 3.4 % at N = 2048).
+template <bool CAUSAL>
+__device__ __forceinline__ int q_row0(const Item& w, int t) {
+  return w.q0 + (CAUSAL ? 1 - t : t) * kBM;
+}
+
 // The m-th work item of this CTA: items are numbered in sections of
 // sec_heads heads (sized so that a section's K and V stay in L2 while its
 // items run) and, inside a section, heaviest first (causal: the Q-tile pairs
 // with the most key tiles), heads inner; they are dealt in snake order (round
 // m goes left to right when m is even, right to left when odd).  Returns
 // false past the last item.
-struct Item {
-  int q0, bh, n[2], nt;
-};
-
 template <bool CAUSAL>
 __device__ __forceinline__ bool get_item(int m, int N, int BH, int sec_heads, Item& w) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
@@ -111,7 +123,7 @@ __device__ __forceinline__ bool get_item(int m, int N, int BH, int sec_heads, It
   const int n_kv = (N + kBN - 1) / kBN;
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    const int qs = w.q0 + t * kBM;
+    const int qs = q_row0<CAUSAL>(w, t);
     w.n[t] = qs >= N ? 0 : (CAUSAL ? min(n_kv, qs / kBN + 1) : n_kv);
   }
   w.nt = max(w.n[0], w.n[1]);
@@ -200,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int m = 0; ok && get_item<CAUSAL>(m, N, BH, args.sec_heads, w); ++m) {
       const int nj = w.n[t];
       if (nj == 0) continue;
-      const int qs = w.q0 + t * kBM;
+      const int qs = q_row0<CAUSAL>(w, t);
       const int row = qs + r_tile;
       float m_ref = -INFINITY;  // running reference max, log2 units
       float l = 0.f;            // sum of the fp32 probabilities (gives L)
@@ -558,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (w.n[t] == 0) continue;
           for (int cc = 0; cc < C::kChunks; ++cc)
             tma_load_3d_w(sbase + C::kQOff + t * C::kTileBytes + cc * C::kChunkBytes, &tm_q,
-                          b.q_full, cc * C::kChunkElems, w.q0 + t * kBM, w.bh);
+                          b.q_full, cc * C::kChunkElems, q_row0<CAUSAL>(w, t), w.bh);
         }
         items = m + 1;
         bool aborted = false;
