@@ -20,7 +20,8 @@
 // step counter across items, so the next item's first loads and MMAs start
 // while this item's last dQ tile drains and its dK/dV are written out: V is
 // released after the item's last dP^T, K after its last dQ, and dK/dV go from
-// TMEM straight to global memory (the K/V tiles are already being refilled).
+// TMEM to global memory through the warps' own parts of the dS buffer (the
+// K/V tiles are already being refilled), in whole 128-byte row segments.
 //
 // The global reduce-adds of dQ are capped per SM (about 25 bytes/cycle
 // measured on GB300, whatever the path), so a 64 KiB dQ tile costs ~2600

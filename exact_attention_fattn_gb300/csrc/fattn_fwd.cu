@@ -13,7 +13,8 @@
 // and O/l, L are written once at the end.
 //
 // Persistent: one CTA per SM walks work items, each a pair of Q tiles (rows
-// [256*pair, 256*pair + 256)) of one (batch, head).  Items are numbered
+// [256*pair, 256*pair + 256)) of one (batch, head); with the causal mask
+// tile 0 is the upper half (see q_row0).  Items are numbered
 // heaviest first (causal: the pairs with the most key tiles) and dealt to the
 // CTAs in snake order, so that every CTA gets a similar total; the next item's
 // Q load and first S MMAs overlap the current item's last steps and
