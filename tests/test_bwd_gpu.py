@@ -34,6 +34,10 @@ SMALL = [
     (1, 2, 640, 128, True),
     (1, 2, 1000, 128, False),
     (1, 1, 511, 64, False),
+    # causal, even tile counts: every head dealt K/V tile by K/V tile
+    # (small grids), and 64 paired heads followed by 16 single-tile heads
+    (2, 4, 1024, 64, True),
+    (4, 20, 512, 128, True),
 ]
 
 
