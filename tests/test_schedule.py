@@ -109,3 +109,26 @@ def test_schedule_rejects_bad_arguments():
     assert lib.fattn_bwd_schedule(1, 1, 128, 96, 1, 0, 1, L2, buf, None) == _lib.FATTN_ERR_UNSUPPORTED
     assert lib.fattn_bwd_schedule(1, 1, 128, 128, 1, 0, 1, L2, buf, None) == _lib.FATTN_OK
     assert buf[0] == 0
+
+
+def test_schedule_fuzz():
+    """Seeded random shapes, masks, modes and grids: every K/V tile exactly
+    once, shares summing to the total walk."""
+    import random
+
+    rng = random.Random(20261202)
+    for _ in range(60):
+        B = rng.randint(1, 4)
+        H = rng.randint(1, 40)
+        N = rng.choice([1, 127, 128, 129, 256, 384, 1000, 2048, 2176, 4096, 8192])
+        d = rng.choice([64, 128])
+        causal = rng.random() < 0.7
+        det = rng.random() < 0.2
+        n_tiles = math.ceil(N / 128)
+        items = B * H * n_tiles
+        grid = rng.randint(1, min(SMS, items))
+        l2 = rng.choice([0, 32 * 2**20, L2])
+        item_cta, q_tiles = fattn_bwd_schedule(B, H, N, d, causal, grid, l2, deterministic=det)
+        assert item_cta.min().item() >= 0, (B, H, N, d, causal, det, grid, l2)
+        assert item_cta.max().item() < grid
+        assert q_tiles.sum().item() == B * H * sum(walk(n_tiles, causal))
