@@ -43,3 +43,22 @@ def test_exp2_cubic_error_in_fp32():
     for n in (-100, -10, 0, 3):
         y = np.ldexp(p.astype(np.float64), n)
         assert (np.abs(y / np.exp2(f.astype(np.float64) + n) - 1.0)).max() < 7.6e-5
+
+
+def test_microbench_sources_compile(tmp_path):
+    """Every committed microbenchmark compiles for sm_103a (object only; no GPU)."""
+    import shutil
+    import subprocess
+
+    import pytest
+
+    nvcc = shutil.which("nvcc") or ("/usr/local/cuda/bin/nvcc"
+                                    if os.path.exists("/usr/local/cuda/bin/nvcc") else None)
+    if nvcc is None:
+        pytest.skip("nvcc not available")
+    for name, src in mb.PROGRAMS.items():
+        cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
+               "--expt-relaxed-constexpr", "-c", os.path.join(mb.HERE, src),
+               "-o", str(tmp_path / (name + ".o"))]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        assert r.returncode == 0, f"{src}: {r.stderr[-2000:]}"
