@@ -23,6 +23,7 @@ from .attention import (  # noqa: F401
     attention_forward,
     attention_forward_rows,
     attention_lse_all_rows,
+    attention_abs_weighted_values,
     attention_backward,
     attention_backward_query_rows,
     attention_backward_key_rows,

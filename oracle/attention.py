@@ -224,6 +224,40 @@ def attention_lse_all_rows(q, k, causal: bool, scale: float, row_chunk: int = 20
     return lse.reshape(lead + lse.shape[1:])
 
 
+def attention_abs_weighted_values(q, k, v, causal: bool, scale: float, rows=None,
+                                  row_chunk: int = 2048):
+    """A[i, c] = sum_j P_ij |V_jc|, with P = softmax(scale Q K^T) as in
+    attention_forward [V1详解 §1.1]: the softmax average of |V| per row.
+
+    Not a quantity of the method itself: it is the scale of the error that
+    rounding the probabilities to a 16-bit format before the P V product
+    adds to O (each P_ij carries a relative error of at most 2^-9 in bf16, so
+    O_ic moves by at most 2^-9 (A_ic + |O_ic|) once normalised; the derivation
+    is with the tolerances).  ``rows`` as in attention_forward_rows (None:
+    every row).  Returns [..., R, d].
+    """
+    q, k, v = to_f64(q), to_f64(k), to_f64(v)
+    qh, lead = _heads(q)
+    kh, _ = _heads(k)
+    vh, _ = _heads(v)
+    n = qh.shape[1]
+    if rows is None:
+        rows_all = np.arange(n)
+        per_head = None
+    else:
+        rows_all = np.asarray(rows)
+        per_head = rows_all.reshape(-1, rows_all.shape[-1]) if rows_all.ndim > 1 else None
+    r = rows_all.shape[-1]
+    out = np.empty((qh.shape[0], r, vh.shape[2]))
+    for h in range(qh.shape[0]):
+        rr = per_head[h] if per_head is not None else rows_all
+        for r0 in range(0, r, row_chunk):
+            sub = rr[r0:r0 + row_chunk]
+            p = _softmax_rows(_scores(qh[h], kh[h], sub, causal, float(scale)))[0]
+            out[h, r0:r0 + len(sub)] = p @ np.abs(vh[h])
+    return out.reshape(lead + out.shape[1:])
+
+
 # --------------------------------------------------------------------------
 # attention backward: the gradient formulas
 # --------------------------------------------------------------------------

@@ -28,3 +28,20 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """One line per parity check that ran: the errors against the oracle."""
+    try:
+        from tolerances import REPORT
+    except ImportError:
+        return
+    if not REPORT:
+        return
+    terminalreporter.section("parity against the fp64 oracle (max / mean abs error)")
+    for test, what, fig in REPORT:
+        extra = " ".join(f"{k}={v:.3e}" if isinstance(v, float) else f"{k}={v}"
+                         for k, v in fig.items() if k not in ("max", "mean"))
+        terminalreporter.write_line(
+            f"{test.split('::')[-1]:<60} {what:<14} max {fig['max']:.3e}  "
+            f"mean {fig['mean']:.3e}  {extra}")

@@ -330,6 +330,40 @@ def check_row_subsets(o):
         assert np.abs(lall - lse).max() <= 1e-14
 
 
+def check_abs_weighted_values(o):
+    """sum_j P_ij |V_jc| (the scale of the P-rounding term in the O
+    tolerance): with every V entry >= 0 it is O itself; with one key's value
+    row e_c and the others zero it is that key's softmax weight (causal row
+    0: exactly 1); with V of one sign flipped it does not change; and it
+    bounds |O| from above.  Rows variant = full computation."""
+    r = _rng(13)
+    q, k = (r.standard_normal((1, 2, 17, 4)) for _ in range(2))
+    v = r.standard_normal((1, 2, 17, 4))
+    for causal in (False, True):
+        a = o.attention_abs_weighted_values(q, k, v, causal, 0.6, row_chunk=5)
+        out, _ = o.attention_forward(q, k, np.abs(v), causal, 0.6)
+        assert np.abs(a - out).max() <= 1e-14
+        assert np.abs(o.attention_abs_weighted_values(q, k, -v, causal, 0.6) - a).max() <= 1e-14
+        signed, _ = o.attention_forward(q, k, v, causal, 0.6)
+        assert (np.abs(signed) <= a + 1e-14).all()
+        onehot = np.zeros_like(v)
+        onehot[:, :, 0, 2] = -3.0
+        a1 = o.attention_abs_weighted_values(q, k, onehot, causal, 0.6)
+        s = 0.6 * np.einsum("bhid,bhjd->bhij", q, k)
+        if causal:
+            s = np.where(np.tril(np.ones((17, 17), bool)), s, -np.inf)
+        p = np.exp(s - s.max(-1, keepdims=True))
+        p /= p.sum(-1, keepdims=True)
+        assert np.abs(a1[..., 2] - 3.0 * p[..., 0]).max() <= 1e-14
+        assert np.abs(a1[..., [0, 1, 3]]).max() == 0.0
+        if causal:
+            assert a1[0, 0, 0, 2] == 3.0
+        rows = np.array([[0, 5, 16], [2, 3, 9]])
+        ar = o.attention_abs_weighted_values(q, k, v, causal, 0.6, rows=rows[None])
+        for h in range(2):
+            assert np.abs(ar[0, h] - a[0, h, rows[h]]).max() <= 1e-14
+
+
 ALL_CHECKS = [
     check_worked_example,
     check_three_pass_vs_library,
@@ -344,4 +378,5 @@ ALL_CHECKS = [
     check_backward_identities,
     check_tiled_algorithms,
     check_row_subsets,
+    check_abs_weighted_values,
 ]

@@ -75,13 +75,13 @@ def test_fwd_medium_d64_full():
     check_l(to_np(lse), l_ref)
 
 
-@pytest.mark.parametrize("w,rows", [(W.CAUSAL_OUTLIERS, 48), (W.LONG_CAUSAL, 256)]
-                         + [(W.SWEEP_D128.with_n(n), 48) for n in W.SWEEP_NS]
-                         + [(W.Workload("b8h32_n4096_d64_sections", 8, 32, 4096, 64, False,
-                                        backward=False, seed=1010), 8)])
+@pytest.mark.parametrize("w,rows", [(W.Workload("b8h32_n4096_d64_sections", 8, 32, 4096, 64,
+                                                False, backward=False, seed=1010), 8)])
 def test_fwd_full_size_sampled_rows(w, rows):
-    """Full-size launch; the oracle evaluates a seeded sample of rows per head
-    (always including the first and the last row)."""
+    """Full-size launch with 256 heads in several L2 head sections; the oracle
+    evaluates a seeded sample of rows per head (always including the first
+    and the last row).  The measured workloads are compared element by
+    element in test_full_size_gpu.py."""
     inp = W.make_inputs(w, with_grad=False)
     o, lse = run_fwd(inp, w.causal, w.scale)
     r = W.sample_rows(w, rows, seed=w.seed + 1)
