@@ -107,7 +107,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", gpu_id],
+                 "-lms", "20", "-i", gpu_id],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             return
@@ -436,12 +436,25 @@ def run_fattn(args, w):
     dom_ms = per_stage[dominant]
     achieved = stage_flops.get(dominant, 0.0) / (dom_ms * 1e-3) / 1e12
     traffic = load_traffic(dominant, w.name)
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sustained"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sustained"],
+    # The timed region lasts steps x ms_per_step (tens of ms at the default
+    # step count), far shorter than the seconds-long loop behind the
+    # sustained figure, so the burst peak is the denominator; the sustained
+    # one only applies to a region of a second or more.
+    region_s = total_ms * 1e-3
+    peak_key = "bf16_sustained" if region_s >= 1.0 else "bf16"
+    peak_kind = "sustained" if peak_key == "bf16_sustained" else "burst"
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks[peak_key],
+                "unit": "TFLOP/s", "frac": achieved / peaks[peak_key],
                 "traffic": traffic, "kernel": dominant,
-                "peak_kind": f"bf16 dense, sustained ({peaks['source']})",
-                "frac_of_burst_peak": achieved / peaks["bf16"]}
+                "peak_kind": f"bf16 dense, {peak_kind} ({peaks['source']}); timed region "
+                             f"{region_s * 1e3:.1f} ms",
+                "frac_of_sustained_peak": achieved / peaks["bf16_sustained"]}
     fwd_tf = base / (per_stage["fwd"] * 1e-3) / 1e12
+    roofline_fwd = {"bound": "tensor", "achieved": fwd_tf, "peak": peaks[peak_key],
+                    "unit": "TFLOP/s", "frac": fwd_tf / peaks[peak_key],
+                    "traffic": load_traffic("fwd", w.name), "kernel": "fwd",
+                    "peak_kind": roofline["peak_kind"],
+                    "gate": "forward at >= 0.60 of the dense bf16 peak on this workload"}
     bwd_ms = per_stage["bwd_prepare"] + per_stage["bwd_main"] + per_stage["bwd_finish"]
     bwd_tf = bwd / (bwd_ms * 1e-3) / 1e12
     line = {
@@ -464,6 +477,7 @@ def run_fattn(args, w):
         "frac_of_spec_peak": value / world / spec_tflops(dev, clocks),
         "frac_of_spec_peak_note": "per-GPU value / (SMs x 8192 FLOP/clk/SM x max SM clock)",
         "roofline": roofline,
+        "roofline_fwd": roofline_fwd,
         "clocks": clocks,
         "gpu_launches": args.steps * len(stages),
         "e2e": e2e,
