@@ -46,6 +46,8 @@ SIGNATURES = {
                                    _c_int, _c_int, _c_int, _c_float, _vp]),
     "fattn_bwd_schedule": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                     ctypes.c_longlong, _vp, _vp]),
+    "fattn_bwd_schedule_items": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                          ctypes.c_longlong, _vp, _vp]),
     "fattn_check_status": (_c_int, [_vp]),
     "fattn_status_string": (ctypes.c_char_p, [_c_int]),
     "fattn_set_wait_budget": (None, [ctypes.c_longlong]),

@@ -246,6 +246,22 @@ def fattn_bwd_schedule(B: int, H: int, N: int, d: int, causal: bool, grid: int, 
     return item_cta.view(B * H, n_tiles), cta_q_tiles
 
 
+def fattn_bwd_schedule_items(B: int, H: int, N: int, d: int, causal: bool, grid: int,
+                             l2_bytes: int, deterministic: bool = False):
+    """The backward schedule in processing order (host only): a list, per CTA,
+    of its items (bh, j, i0, n_it, rot) in the order it runs them."""
+    n_items = B * H * ((N + 127) // 128)
+    start = torch.empty(max(grid, 0) + 1, dtype=torch.int32)
+    items = torch.empty(5 * n_items, dtype=torch.int32)
+    rc = _lib.load().fattn_bwd_schedule_items(B, H, N, d, int(bool(causal)),
+                                              int(bool(deterministic)), grid, l2_bytes,
+                                              start.data_ptr(), items.data_ptr())
+    _lib.check("fattn_bwd_schedule_items", rc)
+    it = items.view(n_items, 5).tolist()
+    st = start.tolist()
+    return [[tuple(e) for e in it[st[c]:st[c + 1]]] for c in range(grid)]
+
+
 def fattn_check_status(device=None) -> int:
     """Synchronise the current stream and return (and clear) the status."""
     dev = torch.device("cuda") if device is None else torch.device(device)

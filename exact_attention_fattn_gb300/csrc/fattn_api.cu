@@ -6,12 +6,23 @@
 
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/fattn.h"
 #include "fattn_internal.h"
 #include "fattn_ptx.cuh"
 #include "fattn_sched.h"
 
 namespace fattn {
+
+// An NVTX range around each entry point that enqueues work, so that
+// profiler timelines show the library's calls (no cost without a tool).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // The single status word of the library on each device.
 __device__ DeviceStatus g_status;
@@ -26,6 +37,7 @@ DeviceStatus* g_status_ptr[kMaxDevices] = {};
 int g_arch_ok[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 unsupported
 long long g_budget = kDefaultBudget;
 float g_tau_log2 = 8.0f;
+constexpr float kFp8TauMax = 8.0f;
 bool g_deterministic = false;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -139,6 +151,7 @@ extern "C" {
 
 int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
               int N, int d, int causal, float scale, fattn_stream_t stream) {
+  const NvtxRange nvtx_range("fattn_fwd");
   int rc = check_sizes(B, H, N, d);
   if (rc != FATTN_OK) return rc;
   if (!q || !k || !v || !o || !lse) return FATTN_ERR_INVALID_ARG;
@@ -177,6 +190,7 @@ size_t fattn_fp8_codes_bytes(int B, int H, int N, int d, int transposed) {
 
 int fattn_quantize_fp8(const void* x, void* codes, float* scales, int B, int H, int N, int d,
                        int transposed, fattn_stream_t stream) {
+  const NvtxRange nvtx_range("fattn_quantize_fp8");
   int rc = check_sizes(B, H, N, d);
   if (rc != FATTN_OK) return rc;
   if (d != 128) return FATTN_ERR_UNSUPPORTED;
@@ -191,6 +205,7 @@ int fattn_quantize_fp8(const void* x, void* codes, float* scales, int B, int H, 
 
 int fattn_quantize_fp8_rotated(const void* x, const float* signs, void* codes, float* scales,
                                int B, int H, int N, int d, fattn_stream_t stream) {
+  const NvtxRange nvtx_range("fattn_quantize_fp8_rotated");
   int rc = check_sizes(B, H, N, d);
   if (rc != FATTN_OK) return rc;
   if (d != 128) return FATTN_ERR_UNSUPPORTED;
@@ -207,6 +222,7 @@ int fattn_quantize_fp8_rotated(const void* x, const float* signs, void* codes, f
 int fattn_fwd_fp8(const void* q8, const float* sq, const void* k8, const float* sk,
                   const void* v8t, const float* sv, void* o, float* lse, int B, int H, int N,
                   int d, int causal, float scale, fattn_stream_t stream) {
+  const NvtxRange nvtx_range("fattn_fwd_fp8");
   int rc = check_sizes(B, H, N, d);
   if (rc != FATTN_OK) return rc;
   if (d != 128) return FATTN_ERR_UNSUPPORTED;
@@ -237,7 +253,9 @@ int fattn_fwd_fp8(const void* q8, const float* sq, const void* k8, const float* 
   {
     std::lock_guard<std::mutex> lock(g_mu);
     a.wait_budget = g_budget;
-    a.tau_log2 = g_tau_log2;
+    // The e4m3 probabilities P * rho reach 2^tau (rho <= 1); e4m3 saturates
+    // at 448 = 2^8.81, so the FP8 forward never lets tau above 8.
+    a.tau_log2 = g_tau_log2 > kFp8TauMax ? kFp8TauMax : g_tau_log2;
   }
   return from_cuda(launch_fwd_fp8(causal != 0, tq, tk, tv, a,
                                   reinterpret_cast<cudaStream_t>(stream)));
@@ -276,6 +294,7 @@ size_t fattn_bwd_workspace_bytes(int B, int H, int N, int d) {
 
 int fattn_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_accum, int B, int H,
                          int N, int d, fattn_stream_t stream) {
+  const NvtxRange nvtx_range("fattn_bwd_preprocess");
   int rc = check_sizes(B, H, N, d);
   if (rc != FATTN_OK) return rc;
   if (!o || !dO || !D || !dq_accum) return FATTN_ERR_INVALID_ARG;
@@ -356,6 +375,7 @@ extern "C" {
 int fattn_bwd_prepare(const void* o, const void* dO, const float* lse, void* workspace,
                       size_t workspace_bytes, int B, int H, int N, int d,
                       fattn_stream_t stream) {
+  const NvtxRange nvtx_range("fattn_bwd_prepare");
   int rc = check_sizes(B, H, N, d);
   if (rc != FATTN_OK) return rc;
   if (!o || !dO || !lse) return FATTN_ERR_INVALID_ARG;
@@ -370,6 +390,7 @@ int fattn_bwd_prepare(const void* o, const void* dO, const float* lse, void* wor
 int fattn_bwd_main(const void* q, const void* k, const void* v, const void* dO, void* workspace,
                    size_t workspace_bytes, void* dk, void* dv, int B, int H, int N, int d,
                    int causal, float scale, fattn_stream_t stream) {
+  const NvtxRange nvtx_range("fattn_bwd_main");
   int rc = check_sizes(B, H, N, d);
   if (rc != FATTN_OK) return rc;
   if (!q || !k || !v || !dO || !dk || !dv) return FATTN_ERR_INVALID_ARG;
@@ -386,6 +407,7 @@ int fattn_bwd_main(const void* q, const void* k, const void* v, const void* dO, 
 
 int fattn_bwd_finish(const void* workspace, size_t workspace_bytes, void* dq, int B, int H, int N,
                      int d, float scale, fattn_stream_t stream) {
+  const NvtxRange nvtx_range("fattn_bwd_finish");
   int rc = check_sizes(B, H, N, d);
   if (rc != FATTN_OK) return rc;
   if (!dq || !aligned16(dq)) return FATTN_ERR_INVALID_ARG;
@@ -400,6 +422,7 @@ int fattn_bwd(const void* q, const void* k, const void* v, const void* o, const 
               const float* lse, void* dq, void* dk, void* dv, void* workspace,
               size_t workspace_bytes, int B, int H, int N, int d, int causal, float scale,
               fattn_stream_t stream) {
+  const NvtxRange nvtx_range("fattn_bwd");
   int rc = check_sizes(B, H, N, d);
   if (rc != FATTN_OK) return rc;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FATTN_ERR_INVALID_ARG;
@@ -430,6 +453,9 @@ int fattn_bwd_schedule(int B, int H, int N, int d, int causal, int deterministic
   BwdArgs a{};
   a.N = N;
   a.BH = BH;
+  // The item function only tests the counter pointer against null.
+  uint32_t dummy_order = 0;
+  a.dq_order = deterministic ? &dummy_order : nullptr;
   plan_bwd_schedule(a, n_tiles, d, causal != 0, deterministic != 0, grid, l2_bytes);
   for (long long i = 0; i < items; ++i) item_cta[i] = -1;
   for (int c = 0; c < grid; ++c) {
@@ -448,7 +474,45 @@ int fattn_bwd_schedule(int B, int H, int N, int d, int causal, int deterministic
   return FATTN_OK;
 }
 
+int fattn_bwd_schedule_items(int B, int H, int N, int d, int causal, int deterministic, int grid,
+                             long long l2_bytes, int* cta_start, int* items) {
+  const int rc = check_sizes(B, H, N, d);
+  if (rc != FATTN_OK) return rc;
+  if (grid <= 0 || l2_bytes < 0 || !cta_start || !items) return FATTN_ERR_INVALID_ARG;
+  const int BH = B * H;
+  const int n_tiles = (N + 127) / 128;
+  const long long n_items = static_cast<long long>(n_tiles) * BH;
+  if (n_items > (1ll << 24) || grid > n_items) return FATTN_ERR_INVALID_ARG;
+  BwdArgs a{};
+  a.N = N;
+  a.BH = BH;
+  uint32_t dummy_order = 0;
+  a.dq_order = deterministic ? &dummy_order : nullptr;
+  plan_bwd_schedule(a, n_tiles, d, causal != 0, deterministic != 0, grid, l2_bytes);
+  long long e = 0;
+  for (int c = 0; c < grid; ++c) {
+    cta_start[c] = static_cast<int>(e);
+    BwdItem w;
+    for (int m = 0; m <= n_items; ++m) {
+      const bool more = causal ? bwd_item<true>(m, n_tiles, a, grid, c, w)
+                               : bwd_item<false>(m, n_tiles, a, grid, c, w);
+      if (!more) break;
+      if (e >= n_items) return FATTN_ERR_INVALID_ARG;   // more entries than items: not a schedule
+      int* out = items + 5 * e;
+      out[0] = w.bh;
+      out[1] = w.j;
+      out[2] = w.i0;
+      out[3] = w.n_it;
+      out[4] = w.rot;
+      ++e;
+    }
+  }
+  cta_start[grid] = static_cast<int>(e);
+  return FATTN_OK;
+}
+
 int fattn_check_status(fattn_stream_t stream) {
+  const NvtxRange nvtx_range("fattn_check_status");
   DeviceStatus* status = nullptr;
   int rc = device_setup(&status);
   if (rc != FATTN_OK) return rc;
@@ -523,6 +587,7 @@ extern "C" int fattn_bwd_noalloc(const void* q, const void* k, const void* v, co
                                  const void* dO, const float* lse, void* dq, void* dk, void* dv,
                                  int B, int H, int N, int d, int causal, float scale,
                                  fattn_stream_t stream) {
+  const fattn::NvtxRange nvtx_range("fattn_bwd_noalloc");
   int rc = check_sizes(B, H, N, d);
   if (rc != FATTN_OK) return rc;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FATTN_ERR_INVALID_ARG;

@@ -717,7 +717,28 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   const dim3 grid(static_cast<unsigned>(items < sms ? items : sms));
   BwdArgs ab = a;
   plan_bwd_schedule(ab, n_tiles, HD, CAUSAL, a.dq_order != nullptr, static_cast<int>(grid.x), l2);
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tacc, ab);
+  if (a.dq_order == nullptr) {
+    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tacc, ab);
+    return cudaGetLastError();
+  }
+  // Ordered mode: a CTA waits for dQ adds of CTAs holding smaller K/V tiles,
+  // so every CTA of the grid must be resident at once.  A cooperative launch
+  // guarantees that (or fails up front) even when other work shares the GPU.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tdo, tacc, ab);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return e;
+  }
   return cudaGetLastError();
 }
 

@@ -235,6 +235,23 @@ int fattn_bwd_schedule(int B, int H, int N, int d, int causal, int deterministic
                        long long l2_bytes, int* item_cta, long long* cta_q_tiles);
 
 /*
+ * The same schedule in processing order, for checking it on the host (no
+ * GPU): every CTA's work items in the order it runs them, with the Q tiles
+ * each item visits.  The ordered dQ reduction of the deterministic mode
+ * waits, at every Q tile, for the smaller K/V tiles of the head; whether
+ * such a schedule can always make progress is a property of this order.
+ *   B .. l2_bytes : as for fattn_bwd_schedule
+ *   cta_start     : out, int [grid + 1], host memory: CTA c's items are
+ *                   entries cta_start[c] .. cta_start[c + 1] - 1 of items
+ *   items         : out, int [5 * B*H*n_tiles], host memory: per entry
+ *                   (bh, j, i0, n_it, rot); step it of the item visits Q tile
+ *                   i0 + it when causal, (rot + it) mod n_tiles otherwise
+ * Returns as fattn_bwd_schedule (NULL cta_start or items: invalid).
+ */
+int fattn_bwd_schedule_items(int B, int H, int N, int d, int causal, int deterministic, int grid,
+                             long long l2_bytes, int* cta_start, int* items);
+
+/*
  * Synchronise `stream`, then report the first error since the last call:
  * a pending asynchronous CUDA error (FATTN_ERR_CUDA) or a kernel wait
  * timeout recorded on the current device (FATTN_ERR_TIMEOUT).  Clears the
@@ -274,7 +291,9 @@ void fattn_set_deterministic(int on);
  * then.  The result is exact for any tau_log2 >= 0 because l and O always
  * share the reference; probabilities stay <= 2^tau_log2.  Default 8
  * (log2 256, the page's value).  Negative values restore the default;
- * values above 16 are clamped to 16.  Applies to later launches.
+ * values above 16 are clamped to 16.  The FP8 forward uses at most 8: its
+ * probabilities are rounded to e4m3, which saturates at 448 = 2^8.81, so a
+ * larger threshold would clip them.  Applies to later launches.
  */
 void fattn_set_rescale_threshold(float tau_log2);
 

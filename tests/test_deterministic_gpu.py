@@ -100,3 +100,44 @@ def test_deterministic_repeats_on_the_benchmark_shape():
                     assert torch.equal(a, b), f"run {it}: {name} differs"
     finally:
         A.fattn_set_deterministic(False)
+
+
+def test_deterministic_with_concurrent_work_on_the_gpu():
+    """The ordered backward waits on dQ adds of other CTAs of its grid, so all
+    of them must be resident at once.  It is launched cooperatively: while a
+    side stream keeps the SMs busy with matrix products, the result is either
+    bit-identical to an uncontended run or a clean launch error, never a wait
+    timeout.  The wait budget is cut to ~1/60 s for the test, so a grid that
+    started only partly would time out well within it."""
+    w = W.Workload("det_busy", 2, 32, 2048, 128, True, seed=612)
+    inp = W.make_inputs(w)
+    o, lse = run_fwd(inp, True, w.scale)
+    ws = A.workspace_for(o)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    a = torch.randn(8192, 8192, device="cuda", dtype=torch.bfloat16)
+    side = torch.cuda.Stream()
+    A.fattn_set_deterministic(True)
+    A.fattn_set_wait_budget(1 << 25)
+    try:
+        ref = _bwd(inp, True, w.scale, o, lse, ws)
+        ref = tuple(t.clone() for t in ref)
+        for trial in range(3):
+            torch.cuda.synchronize()
+            with torch.cuda.stream(side):
+                for _ in range(60):
+                    a = (a @ a).mul_(1e-4)
+            try:
+                got = A.fattn_bwd(q, k, v, o, do, lse, causal=True, scale=w.scale, workspace=ws)
+            except RuntimeError as exc:          # refused up front: acceptable
+                assert "CUDA error" in str(exc), str(exc)
+                torch.cuda.synchronize()
+                continue
+            status = A.fattn_check_status()
+            torch.cuda.synchronize()
+            assert status == 0, f"trial {trial}: status {status}"
+            for x, y, name in zip(got, ref, ("dQ", "dK", "dV")):
+                assert torch.equal(x, y), f"trial {trial}: {name} differs"
+    finally:
+        A.fattn_set_wait_budget(0)
+        A.fattn_set_deterministic(False)
+        torch.cuda.synchronize()

@@ -10,7 +10,7 @@ import os
 import pytest
 
 from exact_attention_fattn_gb300 import _lib
-from exact_attention_fattn_gb300.attention import fattn_bwd_schedule
+from exact_attention_fattn_gb300.attention import fattn_bwd_schedule, fattn_bwd_schedule_items
 
 L2 = 126 * 2**20  # an L2 of GB300's size (the head sections are sized from it)
 SMS = 152
@@ -132,3 +132,84 @@ def test_schedule_fuzz():
         assert item_cta.min().item() >= 0, (B, H, N, d, causal, det, grid, l2)
         assert item_cta.max().item() < grid
         assert q_tiles.sum().item() == B * H * sum(walk(n_tiles, causal))
+
+
+# ---------------------------------------------------------------------------
+# The ordered (deterministic) dQ reduction: the reduce warp of the CTA that
+# holds K/V tile j of head bh adds its dQ tile into Q tile i only once tile
+# i's counter shows that K/V tiles 0..j-1 of bh have added theirs, and each
+# CTA serves its steps strictly in order.  With every CTA of the grid
+# resident, that makes progress if and only if the simulation below, which
+# replays exactly those rules on the schedule the kernel runs, finishes.
+
+def visits(entry, n_tiles, causal):
+    bh, j, i0, n_it, rot = entry
+    if causal:
+        return [(bh, i0 + it, j) for it in range(n_it)]
+    return [(bh, (rot + it) % n_tiles, j) for it in range(n_it)]
+
+
+def ordered_reduction_finishes(per_cta, n_tiles, causal):
+    """Replay the counter waits; True if every CTA gets through its steps."""
+    queues = [[v for e in items for v in visits(e, n_tiles, causal)] for items in per_cta]
+    pos = [0] * len(queues)
+    counter = {}
+    pending = sum(len(q) for q in queues)
+    while pending:
+        moved = False
+        for c, q in enumerate(queues):
+            while pos[c] < len(q):
+                bh, i, j = q[pos[c]]
+                if counter.get((bh, i), 0) != j:
+                    break
+                counter[(bh, i)] = j + 1
+                pos[c] += 1
+                pending -= 1
+                moved = True
+        if not moved:
+            return False
+    return True
+
+
+DET_CASES = [
+    (2, 32, 4096, 128, True),
+    (1, 4, 1024, 128, True),
+    (2, 3, 777, 64, False),
+    (1, 2, 1000, 128, False),
+    (2, 32, 2048, 128, True),
+    (4, 8, 1024, 128, False),
+    (1, 16, 16384, 128, True),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", DET_CASES)
+def test_ordered_reduction_always_progresses(B, H, N, d, causal):
+    grid = grid_for(B, H, N)
+    per_cta = fattn_bwd_schedule_items(B, H, N, d, causal, grid, L2, deterministic=True)
+    n_tiles = math.ceil(N / 128)
+    assert sum(len(x) for x in per_cta) == B * H * n_tiles
+    assert ordered_reduction_finishes(per_cta, n_tiles, causal)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_ordered_reduction_fuzz(seed):
+    rng = __import__("random").Random(seed)
+    B, H = rng.randint(1, 4), rng.randint(1, 12)
+    N = rng.randint(1, 3000)
+    d = rng.choice((64, 128))
+    causal = rng.random() < 0.5
+    n_tiles = math.ceil(N / 128)
+    grid = rng.randint(1, min(SMS, B * H * n_tiles))
+    per_cta = fattn_bwd_schedule_items(B, H, N, d, causal, grid, L2, deterministic=True)
+    assert ordered_reduction_finishes(per_cta, n_tiles, causal)
+
+
+def test_the_simulation_detects_a_cycle():
+    """The check itself, on hand-made two-CTA schedules of one head with two
+    K/V tiles (entries (bh, j, i0, n_it, rot), causal visit order)."""
+    # each CTA walks its tile over both Q tiles: progresses
+    assert ordered_reduction_finishes([[(0, 0, 0, 2, 0)], [(0, 1, 0, 2, 0)]], 2, True)
+    # CTA 0 runs tile 1 on Q0 first, which needs tile 0 on Q0 -- last on
+    # CTA 1, behind tile 1 on Q1, which needs tile 0 on Q1 -- last on CTA 0
+    cyc = [[(0, 1, 0, 1, 0), (0, 0, 1, 1, 0)], [(0, 1, 1, 1, 0), (0, 0, 0, 1, 0)]]
+    assert not ordered_reduction_finishes(cyc, 2, True)
