@@ -39,6 +39,7 @@ DEFAULT_WORKLOAD = "b2h32_n4096_d128_causal_outliers"
 KERNEL_SOURCES = {
     "fwd": ("exact_attention_fattn_gb300/csrc/fattn_fwd.cu",),
     "bwd_main": ("exact_attention_fattn_gb300/csrc/fattn_bwd.cu",
+                 "exact_attention_fattn_gb300/csrc/fattn_bwd2.cu",
                  "exact_attention_fattn_gb300/csrc/fattn_sched.h",
                  "exact_attention_fattn_gb300/csrc/fattn_sched.cu"),
     "bwd_prepare": ("exact_attention_fattn_gb300/csrc/fattn_bwd_aux.cu",),

@@ -20,6 +20,7 @@ from .attention import (  # noqa: F401
     fattn_fwd_fp8,
     fattn_quantize_fp8,
     fattn_selftest_timeout,
+    fattn_set_bwd_pair,
     fattn_set_deterministic,
     fattn_set_rescale_threshold,
     fattn_set_wait_budget,

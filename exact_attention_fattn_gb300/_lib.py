@@ -53,6 +53,7 @@ SIGNATURES = {
     "fattn_set_wait_budget": (None, [ctypes.c_longlong]),
     "fattn_set_rescale_threshold": (None, [_c_float]),
     "fattn_set_deterministic": (None, [ctypes.c_int]),
+    "fattn_set_bwd_pair": (None, [ctypes.c_int]),
     "fattn_selftest_timeout": (_c_int, [ctypes.c_longlong, _vp]),
     "fattn_version": (ctypes.c_char_p, []),
 }

@@ -283,6 +283,11 @@ def fattn_set_deterministic(on: bool) -> None:
     _lib.load().fattn_set_deterministic(1 if on else 0)
 
 
+def fattn_set_bwd_pair(on: bool) -> None:
+    """d = 128 backward: CTA pairs (True) or one CTA per K/V tile (False, the default)."""
+    _lib.load().fattn_set_bwd_pair(int(bool(on)))
+
+
 def fattn_selftest_timeout(budget_cycles: int, device=None) -> int:
     dev = torch.device("cuda") if device is None else torch.device(device)
     lib = _lib.load()

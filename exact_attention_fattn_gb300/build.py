@@ -19,8 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libfattn.so")
 BUILD_DIR = os.path.join(PKG, "_build")
-SOURCES = ["fattn_api.cu", "fattn_fwd.cu", "fattn_bwd.cu", "fattn_bwd_aux.cu", "fattn_fp8.cu",
-           "fattn_sched.cu"]
+SOURCES = ["fattn_api.cu", "fattn_fwd.cu", "fattn_bwd.cu", "fattn_bwd2.cu", "fattn_bwd_aux.cu",
+           "fattn_fp8.cu", "fattn_sched.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
          "--expt-relaxed-constexpr"]

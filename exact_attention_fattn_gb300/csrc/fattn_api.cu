@@ -39,6 +39,7 @@ long long g_budget = kDefaultBudget;
 float g_tau_log2 = 8.0f;
 constexpr float kFp8TauMax = 8.0f;
 bool g_deterministic = false;
+bool g_bwd_pair = false;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -340,6 +341,11 @@ int bwd_main_impl(const void* q, const void* k, const void* v, const void* dO, v
   if ((rc = make_map(&tv, v, N, BH, d, 128)) != FATTN_OK) return rc;
   if ((rc = make_map(&tdo, dO, N, BH, d, 128)) != FATTN_OK) return rc;
   if ((rc = make_acc_map(&tacc, wbase + ws.acc_off, N, BH, d)) != FATTN_OK) return rc;
+  bool pair = false;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    pair = g_bwd_pair && !g_deterministic && d == 128;
+  }
   BwdArgs a;
   a.L2 = reinterpret_cast<const float*>(wbase + ws.l2_off);
   a.D = reinterpret_cast<const float*>(wbase + ws.d_off);
@@ -356,6 +362,12 @@ int bwd_main_impl(const void* q, const void* k, const void* v, const void* dO, v
   a.BH = BH;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
+  if (pair) {
+    CUtensorMap tq64, tdo64;
+    if ((rc = make_map(&tq64, q, N, BH, d, 64)) != FATTN_OK) return rc;
+    if ((rc = make_map(&tdo64, dO, N, BH, d, 64)) != FATTN_OK) return rc;
+    return from_cuda(launch_bwd2_main(causal != 0, tq, tq64, tk, tv, tdo, tdo64, tacc, a, st));
+  }
   return from_cuda(launch_bwd_main(d, causal != 0, tq, tk, tv, tdo, tacc, a, st));
 }
 
@@ -550,6 +562,11 @@ void fattn_set_wait_budget(long long cycles) {
 void fattn_set_deterministic(int on) {
   std::lock_guard<std::mutex> lock(g_mu);
   g_deterministic = on != 0;
+}
+
+void fattn_set_bwd_pair(int on) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_bwd_pair = on != 0;
 }
 
 void fattn_set_rescale_threshold(float tau_log2) {

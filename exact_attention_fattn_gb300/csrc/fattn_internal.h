@@ -88,6 +88,13 @@ cudaError_t launch_bwd_main(int d, bool causal, const CUtensorMap& tq, const CUt
                             const CUtensorMap& tv, const CUtensorMap& tdo,
                             const CUtensorMap& tacc, const BwdArgs& a, cudaStream_t stream);
 
+// CTA-pair version of the main backward kernel (d = 128, any-order dQ; see
+// fattn_bwd2.cu).  tq64 / tdo64: views of q and dO with 64-row boxes.
+cudaError_t launch_bwd2_main(bool causal, const CUtensorMap& tq, const CUtensorMap& tq64,
+                             const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                             const CUtensorMap& tdo64, const CUtensorMap& tacc, const BwdArgs& a,
+                             cudaStream_t stream);
+
 cudaError_t launch_dq_convert(const float* dq_accum, void* dq, long long elems, float scale,
                               cudaStream_t stream);
 

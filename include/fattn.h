@@ -285,6 +285,20 @@ void fattn_set_wait_budget(long long cycles);
 void fattn_set_deterministic(int on);
 
 /*
+ * Backward main kernel variant for d = 128 in the default (any-order dQ)
+ * mode ("FlashAttention v1～v4" v4 §4, backward with two cooperating CTAs).
+ * On: pairs of CTAs on two SMs issue every matrix product of the backward
+ * together (M = 256 tiles, each CTA staging half of operand B), exchange
+ * half of dS through distributed shared memory and reduce-add dQ summed
+ * over both CTAs' keys.  Off (the default): one CTA per K/V tile, which
+ * measures faster on GB300 (the pair's per-step hand-offs between SMs cost
+ * more than the shared-memory traffic they save).  Both give the same
+ * gradients up to fp32 summation order.  d = 64 and the deterministic mode
+ * always use one CTA per tile.  Applies to later launches.
+ */
+void fattn_set_bwd_pair(int on);
+
+/*
  * Threshold, in log2 units, of the conditional rescaling in the forward pass
  * ("FlashAttention v1～v4" v4 §3): the reference max of a row moves only when
  * the row max exceeds it by more than tau_log2, and O, l are rescaled only
