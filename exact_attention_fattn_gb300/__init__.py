@@ -13,6 +13,7 @@ from .attention import (  # noqa: F401
     fattn_bwd_prepare,
     fattn_bwd_schedule,
     fattn_bwd_schedule_items,
+    fattn_bwd_pair_schedule_items,
     fattn_bwd_preprocess,
     fattn_bwd_workspace_bytes,
     fattn_check_status,

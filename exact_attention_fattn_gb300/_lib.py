@@ -18,6 +18,7 @@ FATTN_ERR_UNSUPPORTED = 2
 FATTN_ERR_CUDA = 3
 FATTN_ERR_TIMEOUT = 4
 FATTN_ERR_TOO_LARGE = 5
+FATTN_ERR_DEBUG_CHECK = 6
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 _c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
@@ -48,6 +49,8 @@ SIGNATURES = {
                                     ctypes.c_longlong, _vp, _vp]),
     "fattn_bwd_schedule_items": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                           ctypes.c_longlong, _vp, _vp]),
+    "fattn_bwd_pair_schedule_items": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int,
+                                               ctypes.c_longlong, _vp, _vp]),
     "fattn_check_status": (_c_int, [_vp]),
     "fattn_status_string": (ctypes.c_char_p, [_c_int]),
     "fattn_set_wait_budget": (None, [ctypes.c_longlong]),

@@ -262,6 +262,21 @@ def fattn_bwd_schedule_items(B: int, H: int, N: int, d: int, causal: bool, grid:
     return [[tuple(e) for e in it[st[c]:st[c + 1]]] for c in range(grid)]
 
 
+def fattn_bwd_pair_schedule_items(B: int, H: int, N: int, causal: bool, clusters: int,
+                                  l2_bytes: int):
+    """The CTA-pair backward's schedule (host only): per cluster, its units
+    (bh, 2u, i0, n_it, rot) in processing order."""
+    n_units = B * H * (((N + 127) // 128 + 1) // 2)
+    start = torch.empty(max(clusters, 0) + 1, dtype=torch.int32)
+    items = torch.empty(5 * n_units, dtype=torch.int32)
+    rc = _lib.load().fattn_bwd_pair_schedule_items(B, H, N, int(bool(causal)), clusters, l2_bytes,
+                                                   start.data_ptr(), items.data_ptr())
+    _lib.check("fattn_bwd_pair_schedule_items", rc)
+    it = items.view(n_units, 5).tolist()
+    st = start.tolist()
+    return [[tuple(e) for e in it[st[c]:st[c + 1]]] for c in range(clusters)]
+
+
 def fattn_check_status(device=None) -> int:
     """Synchronise the current stream and return (and clear) the status."""
     dev = torch.device("cuda") if device is None else torch.device(device)

@@ -19,6 +19,14 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libfattn.so")
 BUILD_DIR = os.path.join(PKG, "_build")
+# Debug variant for tests: every kernel range-checks its computed shared-
+# memory, TMEM and global indices (a failed check is reported as
+# FATTN_ERR_DEBUG_CHECK, not a trap), and the forward's K/V ring has its
+# minimum depth of two stages, so that the ring phases wrap as often as
+# they can.
+DEBUG_LIB_PATH = os.path.join(PKG, "libfattn_debug.so")
+DEBUG_BUILD_DIR = os.path.join(PKG, "_build_debug")
+DEBUG_FLAGS = ["-DFATTN_DEBUG", "-DFATTN_FWD_STAGES=2"]
 SOURCES = ["fattn_api.cu", "fattn_fwd.cu", "fattn_bwd.cu", "fattn_bwd2.cu", "fattn_bwd_aux.cu",
            "fattn_fp8.cu", "fattn_sched.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -40,19 +48,24 @@ def _inputs_newer(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = False) -> str:
-    """Compile every .cu into libfattn.so next to this file; returns its path."""
+def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = False,
+          debug: bool = False) -> str:
+    """Compile every .cu into libfattn.so next to this file (with debug=True:
+    libfattn_debug.so, the checked variant); returns its path."""
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    build_dir = DEBUG_BUILD_DIR if debug else BUILD_DIR
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
+    extra = DEBUG_FLAGS if debug else []
+    os.makedirs(build_dir, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(INCLUDE, "fattn.h"))
     objs, jobs = [], []
     for src in SOURCES:
         path = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(obj)
         if force or _inputs_newer(obj, [path] + headers):
-            cmd = [nvcc, *ARCH, *FLAGS, "-c", path, "-o", obj]
+            cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", path, "-o", obj]
             if ptxas_verbose:
                 cmd += ["-Xptxas", "-v"]
             jobs.append(cmd)
@@ -67,17 +80,17 @@ def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = Fals
                 sys.stderr.write(r.stdout + r.stderr)
             if r.returncode != 0:
                 raise RuntimeError("nvcc failed: " + " ".join(cmd))
-    if force or jobs or _inputs_newer(LIB_PATH, objs):
-        tmp = LIB_PATH + ".tmp"
+    if force or jobs or _inputs_newer(lib_path, objs):
+        tmp = lib_path + ".tmp"
         cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)
             raise RuntimeError("link failed: " + " ".join(cmd))
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    build(verbose=True, force="--force" in sys.argv, ptxas_verbose="-v" in sys.argv)
-    print(LIB_PATH)
+    print(build(verbose=True, force="--force" in sys.argv, ptxas_verbose="-v" in sys.argv,
+                debug="--debug" in sys.argv))

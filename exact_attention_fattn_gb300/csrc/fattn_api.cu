@@ -523,6 +523,41 @@ int fattn_bwd_schedule_items(int B, int H, int N, int d, int causal, int determi
   return FATTN_OK;
 }
 
+int fattn_bwd_pair_schedule_items(int B, int H, int N, int causal, int clusters,
+                                  long long l2_bytes, int* cluster_start, int* items) {
+  const int rc = check_sizes(B, H, N, 128);
+  if (rc != FATTN_OK) return rc;
+  if (clusters <= 0 || l2_bytes < 0 || !cluster_start || !items) return FATTN_ERR_INVALID_ARG;
+  const int BH = B * H;
+  const int n_tiles = (N + 127) / 128;
+  const long long n_units = static_cast<long long>((n_tiles + 1) / 2) * BH;
+  if (n_units > (1ll << 24) || clusters > n_units) return FATTN_ERR_INVALID_ARG;
+  BwdArgs a{};
+  a.N = N;
+  a.BH = BH;
+  plan_bwd2_schedule(a, n_tiles, causal != 0, clusters, l2_bytes);
+  long long e = 0;
+  for (int c = 0; c < clusters; ++c) {
+    cluster_start[c] = static_cast<int>(e);
+    BwdItem w;
+    for (int m = 0; m <= n_units; ++m) {
+      const bool more = causal ? bwd2_item<true>(m, n_tiles, a, clusters, c, w)
+                               : bwd2_item<false>(m, n_tiles, a, clusters, c, w);
+      if (!more) break;
+      if (e >= n_units) return FATTN_ERR_INVALID_ARG;   // more entries than units: not a schedule
+      int* out = items + 5 * e;
+      out[0] = w.bh;
+      out[1] = w.j;
+      out[2] = w.i0;
+      out[3] = w.n_it;
+      out[4] = w.rot;
+      ++e;
+    }
+  }
+  cluster_start[clusters] = static_cast<int>(e);
+  return FATTN_OK;
+}
+
 int fattn_check_status(fattn_stream_t stream) {
   const NvtxRange nvtx_range("fattn_check_status");
   DeviceStatus* status = nullptr;
@@ -550,6 +585,7 @@ const char* fattn_status_string(int status) {
     case FATTN_ERR_CUDA: return "CUDA error";
     case FATTN_ERR_TIMEOUT: return "kernel wait timed out";
     case FATTN_ERR_TOO_LARGE: return "problem exceeds the built-in scratch of fattn_bwd_noalloc";
+    case FATTN_ERR_DEBUG_CHECK: return "a debug-build range check failed in a kernel";
     default: return "unknown status";
   }
 }

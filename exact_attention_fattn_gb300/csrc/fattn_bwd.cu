@@ -240,6 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t* nl2s =
             reinterpret_cast<const uint32_t*>(smem + C::kLdOff + s * 1024) + col0;
         const uint32_t* ds_vec = nl2s + 128;
+        dcheck(in_range(smem_u32(nl2s), 256, sbase + C::kLdOff, sbase + C::kBarOff) &&
+                   in_range(smem_u32(ds_vec), 256, sbase + C::kLdOff, sbase + C::kBarOff),
+               args.status, 402);
         // ---- P^T = 2^(S^T c - L2) (masked), this half's 64 query columns
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull), ph, wc, kWaitSFull));
         if (!ok) break;
@@ -317,7 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int c16 = (col0 >> 3) + g * 4 + qq;
             const uint32_t addr = ds_base + (c16 >> 3) * 16384 + r * 128 +
                                   (static_cast<uint32_t>((c16 & 7) ^ (r & 7)) << 4);
-            st_shared_v4(addr, pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
+            if (dcheck(in_range(addr, 16, ds_base, ds_base + C::kDsBytes), args.status, 401))
+              st_shared_v4(addr, pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
           }
         }
         tmem_st_wait();
@@ -354,8 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
               const uint32_t c16 = hh * 4 + qq;
-              st_shared_v4(wbuf + lane * 128 + ((c16 ^ (lane & 7)) << 4), pk[4 * qq],
-                           pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
+              const uint32_t a = wbuf + lane * 128 + ((c16 ^ (lane & 7)) << 4);
+              if (dcheck(in_range(a, 16, ds_base, ds_base + C::kDsBytes), args.status, 403))
+                st_shared_v4(a, pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
             }
           }
           __syncwarp();
@@ -366,7 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t c16 = lane & 7;
             const uint4 v = ld_shared_v4(wbuf + lr * 128 + ((c16 ^ (lr & 7)) << 4));
             const int row = kv0 + wq * 32 + lr;
-            if (row < N)
+            const size_t o_idx = (static_cast<size_t>(w.bh) * N + row) * HD + cc * 64 + c16 * 8;
+            if (row < N && dcheck(o_idx + 8 <= static_cast<size_t>(args.BH) * N * HD, args.status, 404))
               *reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * HD + cc * 64 + c16 * 8) = v;
           }
           __syncwarp();
@@ -513,6 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < C::kChunks; ++cc)
           tma_load_3d_w(dst + cc * C::kChunkBytes, &tm_q, qf, cc * 64, q0, wi.bh);
         const size_t vec = static_cast<size_t>(wi.bh) * pitch + q0;
+        dcheck(vec + 128 <= static_cast<size_t>(args.BH) * pitch, args.status, 406);
         bulk_load_1d_w(sbase + C::kLdOff + s * 1024, args.L2 + vec, 512, qf);
         bulk_load_1d_w(sbase + C::kLdOff + s * 1024 + 512, args.D + vec, 512, qf);
         issued_q = step + 1;
@@ -664,6 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait32(d0);
           reg_fence32(d1);
           const uint32_t box0 = stage + (wq * (HD / 32) + ch) * 4096 + lane * 128;
+          dcheck(in_range(box0, 4096 + 128, stage, stage + C::kStageBytes), args.status, 405);
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
             const uint32_t sw = static_cast<uint32_t>(c4 ^ (lane & 7)) << 4;

@@ -93,7 +93,7 @@ constexpr int kDovOff = 180224;     // dO_V
 constexpr int kDsqOff = 196608;     // dS_Q: 256 key rows x 64 queries
 constexpr int kLdOff = 229376;      // 2 x 1 KiB: -L log2(e) [128], D [128]
 constexpr int kBarOff = 231424;
-constexpr int kNumBars = 37;
+constexpr int kNumBars = 36;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kMiscOff + 16;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -130,8 +130,7 @@ enum : int {
   kBStageEmpty = 29, // +stage: the parked dQ has been read by the reduce-adds
   kBLdFull = 31,     // +stage: L / D vectors
   kBMmaDone = 33,
-  kBStaged = 34,     // the 4 warps that send dS to the other CTA have staged it
-  kBDqRead = 35,     // +(step & 1): 4 parking warps have read dQ out of TMEM
+  kBDqRead = 34,     // +(step & 1): 4 parking warps have read dQ out of TMEM
 };
 
 __device__ __forceinline__ int dq_slot(uint32_t step) { return static_cast<int>(step & 1); }
@@ -193,7 +192,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBPLocal), 8);
     mbar_init(bar(kBDsLocal), 8);
     mbar_init(bar(kBEpiDone), 8);
-    mbar_init(bar(kBStaged), 4);
     misc[1] = aligned ? 0u : 1u;
     if (!aligned && atomicCAS(&args.status->code, 0u, 2u) == 0u) args.status->where = 101;
     fence_barrier_init();
@@ -234,7 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // row of this key within the unit (rank 0's keys first).  The warpgroup
     // of this CTA's own half stores into its dS_Q directly; the other stages
     // its 128 rows in the step's Q_S buffer (read by S^T, which has completed
-    // by then) and sends them with one 16 KiB bulk copy to the other CTA.
+    // by then) and sends them to the other CTA with bulk copies, 4 KiB per
+    // warp.
     const int ds_row = static_cast<int>(rank) * kTile + r;
     const bool ds_local = half == static_cast<int>(rank);
     const uint32_t peer = rank ^ 1u;
@@ -254,6 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t* nl2s =
             reinterpret_cast<const uint32_t*>(smem + kLdOff + s * 1024) + col0;
         const uint32_t* ds_vec = nl2s + 128;
+        dcheck(in_range(smem_u32(nl2s), 256, sbase + kLdOff, sbase + kBarOff) &&
+                   in_range(smem_u32(ds_vec), 256, sbase + kLdOff, sbase + kBarOff),
+               args.status, 502);
         ok = __all_sync(0xffffffffu, mbar_wait_cl(bar(kBLdFull + s), (step >> 1) & 1, wc,
                                                   kWaitQFull));
         if (!ok) break;
@@ -332,6 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t row_addr =
               ds_local ? sbase + kDsqOff + static_cast<uint32_t>(ds_row) * 128u
                        : sbase + kStageOff + s * kStageBytes + static_cast<uint32_t>(r) * 128u;
+          dcheck(ds_local ? in_range(row_addr, 128, sbase + kDsqOff, sbase + kLdOff)
+                          : in_range(row_addr, 128, sbase + kStageOff + s * kStageBytes,
+                                     sbase + kStageOff + s * kStageBytes + 16384),
+                 args.status, 501);
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq) {
             const uint32_t c16 = static_cast<uint32_t>(g * 4 + qq);
@@ -342,20 +348,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         fence_proxy_async_smem();
         if (!ds_local) {
-          // The staged rows are rows 128 rank .. + 127 of the other CTA's
-          // dS_Q, with the same swizzle (row & 7 == r & 7).  Once all four
-          // warps have staged theirs (a bounded wait, not a named barrier, so
-          // that a warp that gave up cannot stall the others), one lane
-          // sends them.
+          // This warp's 32 staged rows are rows 128 rank + 32 wq .. + 31 of
+          // the other CTA's dS_Q, with the same swizzle (row & 7 == r & 7):
+          // one 4 KiB bulk copy per warp, as soon as the warp has staged them.
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBStaged));
-          if (wq == 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBStaged), ph, wc, kWaitDsFull));
-            if (!ok) break;
-            if (lane == 0)
-              bulk_copy_to_cluster(map_shared(sbase + kDsqOff + rank * (kTile * 128u), peer),
-                                   sbase + kStageOff + s * kStageBytes, 16384,
-                                   map_shared(bar(kBDsqFull), peer));
+          if (lane == 0) {
+            const uint32_t off = static_cast<uint32_t>(wq) * 4096u;
+            bulk_copy_to_cluster(
+                map_shared(sbase + kDsqOff + rank * (kTile * 128u) + off, peer),
+                sbase + kStageOff + s * kStageBytes + off, 4096, map_shared(bar(kBDsqFull), peer));
           }
         }
         tc_fence_before();
@@ -395,8 +396,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
               const uint32_t c16 = hh * 4 + qq;
-              st_shared_v4(wbuf + lane * 128 + ((c16 ^ (lane & 7)) << 4), pk[4 * qq],
-                           pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
+              const uint32_t a = wbuf + lane * 128 + ((c16 ^ (lane & 7)) << 4);
+              if (dcheck(in_range(a, 16, sbase + kKqOff, sbase + kStageOff), args.status, 503))
+                st_shared_v4(a, pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
             }
           }
           __syncwarp();
@@ -406,7 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t c16 = lane & 7;
             const uint4 v = ld_shared_v4(wbuf + lr * 128 + ((c16 ^ (lr & 7)) << 4));
             const int row = kv0 + wq * 32 + lr;
-            if (row < N)
+            const size_t o_idx = (static_cast<size_t>(w.bh) * N + row) * kHd + cc * 64 + c16 * 8;
+            if (row < N && dcheck(o_idx + 8 <= static_cast<size_t>(args.BH) * N * kHd, args.status, 504))
               *reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * kHd + cc * 64 + c16 * 8) = v;
           }
           __syncwarp();
@@ -569,6 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t lf = bar(kBLdFull + s);
       mbar_arrive_expect_tx_w(lf, 1024);
       const size_t vec = static_cast<size_t>(wi.bh) * pitch + q0;
+      dcheck(vec + 128 <= static_cast<size_t>(args.BH) * pitch, args.status, 506);
       bulk_load_1d_w(sbase + kLdOff + s * 1024, args.L2 + vec, 512, lf);
       bulk_load_1d_w(sbase + kLdOff + s * 1024 + 512, args.D + vec, 512, lf);
       issued = step + 1;
@@ -709,6 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBDqRead + dq_slot(step)));
         const uint32_t box0 = stg + (qb * 4 + 2 * dh) * 4096 + lane * 128;
+        dcheck(in_range(box0, 4096 + 128, stg, stg + kStageBytes), args.status, 505);
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const uint32_t sw = static_cast<uint32_t>(c4 ^ (lane & 7)) << 4;

@@ -62,7 +62,15 @@ struct FwdCfg {
   static constexpr int kChunkBytes = kBM * 128;         // one chunk of a 128-row tile
   static constexpr int kTileBytes = kBM * kRowBytes;
   static constexpr int kKSteps = kRowBytes / 32;        // 32-byte K steps of Q K^T
+#ifdef FATTN_FWD_STAGES
+  // Test builds: a shallower K/V ring, so that its phases wrap more often.
+  // Two stages is the least that works: the MMA order per key tile needs
+  // K_{j+1} while V_j is still held.
+  static constexpr int kStages = FATTN_FWD_STAGES;
+  static_assert(kStages >= 2, "the K/V ring needs two stages");
+#else
   static constexpr int kStages = FP8 ? 8 : (HD == 128 ? 4 : 8);
+#endif
   static constexpr int kQOff = 0;
   static constexpr int kKvOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKvOff + kStages * kTileBytes;
@@ -203,6 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + C::col_s(t);
     const uint32_t tP = tmem + lane_off + C::col_p(t);
     const uint32_t tO = tmem + lane_off + C::col_o(t);
+    dcheck(C::col_s(t) + kBN <= 512 && C::col_o(t) + HD <= 512 && C::col_p(t) + 64 <= 512 &&
+               ((tmem >> 16) & 0xFFFFu) == 0u,
+           args.status, 301);
     float c = args.scale_log2;   // FP8: times the Q and K block scales, per tile pair
     const float tau = args.tau_log2;
     const int n_kv = (N + kBN - 1) / kBN;
@@ -436,16 +447,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int h = 0; h < HD / 64; ++h) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          if (grow0 + j < N) {
-            uint4* dst = reinterpret_cast<uint4*>(
-                             args.o + (static_cast<size_t>(w.bh) * N + grow0 + j) * HD) +
-                         8 * h + li;
+          const size_t o_idx = (static_cast<size_t>(w.bh) * N + grow0 + j) * HD + 64 * h + 8 * li;
+          if (grow0 + j < N &&
+              dcheck(o_idx + 8 <= static_cast<size_t>(BH) * N * HD, args.status, 302)) {
+            uint4* dst = reinterpret_cast<uint4*>(args.o + o_idx);
             *dst = make_uint4(pw[4 * (8 * h + j)], pw[4 * (8 * h + j) + 1],
                               pw[4 * (8 * h + j) + 2], pw[4 * (8 * h + j) + 3]);
           }
         }
       }
-      if (row_ok) args.lse[static_cast<size_t>(w.bh) * N + row] = (m_ref + log2f(l)) * kLn2;
+      if (row_ok && dcheck(static_cast<size_t>(w.bh) * N + row < static_cast<size_t>(BH) * N,
+                           args.status, 303))
+        args.lse[static_cast<size_t>(w.bh) * N + row] = (m_ref + log2f(l)) * kLn2;
     }
   } else if (warp == kMmaWarp) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
@@ -589,6 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx_w(full, C::kTileBytes);
           const CUtensorMap* tm = (i & 1) ? &tm_v : &tm_k;
           const uint32_t dst = sbase + C::kKvOff + s * C::kTileBytes;
+          dcheck(in_range(dst, C::kTileBytes, sbase + C::kKvOff, sbase + C::kBarOff), args.status,
+                 304);
           if (FP8 && (i & 1)) {
             // transposed V: d rows x 128 key bytes starting at key (i/2)*128
             tma_load_3d_w(dst, tm, full, (i >> 1) * kBN, 0, w.bh);

@@ -37,6 +37,18 @@ enum WaitSite : unsigned int {
 };
 
 constexpr unsigned int kStatusTimeout = 4;  // == FATTN_ERR_TIMEOUT
+constexpr unsigned int kStatusDebugCheck = 6;  // == FATTN_ERR_DEBUG_CHECK
+
+// Debug builds (compiled with FATTN_DEBUG) check every computed shared-memory
+// address, TMEM column and global index against its range before use; a
+// failed check records FATTN_ERR_DEBUG_CHECK and the site in the device
+// status word and skips the access (no trap: the GPU stays usable and the
+// host reads the status).  In other builds the checks compile away.
+#ifdef FATTN_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -82,6 +94,25 @@ __device__ __forceinline__ void record_timeout(const WaitCtx& w, unsigned int si
     w.status->where = site;
     w.status->block = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
   }
+}
+
+// True if `ok` (always in non-debug builds); otherwise records the site.
+__device__ __forceinline__ bool dcheck(bool ok, DeviceStatus* st, unsigned int site) {
+  if constexpr (kDebugChecks) {
+    if (!ok) {
+      if (atomicCAS(&st->code, 0u, kStatusDebugCheck) == 0u) {
+        st->where = site;
+        st->block = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+      }
+      return false;
+    }
+  }
+  return true;
+}
+
+// Range helpers for the checks: [addr, addr + bytes) inside [lo, hi).
+__device__ __forceinline__ bool in_range(uint32_t addr, uint32_t bytes, uint32_t lo, uint32_t hi) {
+  return addr >= lo && addr + bytes <= hi;
 }
 
 // Wait until the phase with the given parity of `bar` has completed.

@@ -44,7 +44,9 @@ typedef enum {
   FATTN_ERR_UNSUPPORTED = 2, /* d not in {64,128}, or the device is not sm_103 */
   FATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
   FATTN_ERR_TIMEOUT = 4,     /* a kernel gave up on a pipeline wait */
-  FATTN_ERR_TOO_LARGE = 5    /* the problem needs more scratch than fattn_bwd_noalloc has */
+  FATTN_ERR_TOO_LARGE = 5,   /* the problem needs more scratch than fattn_bwd_noalloc has */
+  FATTN_ERR_DEBUG_CHECK = 6  /* debug builds only (FATTN_DEBUG): a kernel found an index out of
+                                its range, skipped the access and recorded the site */
 } fattn_status;
 
 /*
@@ -250,6 +252,23 @@ int fattn_bwd_schedule(int B, int H, int N, int d, int causal, int deterministic
  */
 int fattn_bwd_schedule_items(int B, int H, int N, int d, int causal, int deterministic, int grid,
                              long long l2_bytes, int* cta_start, int* items);
+
+/*
+ * The schedule of the CTA-pair backward (fattn_set_bwd_pair; d = 128), on
+ * the host: per cluster of two CTAs, its work units in processing order.  A
+ * unit is K/V tiles 2u (rank 0) and 2u + 1 (rank 1) of one head.
+ *   B, H, N, causal, l2_bytes : as for fattn_bwd_schedule
+ *   clusters      : number of CTA pairs of the launch
+ *   cluster_start : out, int [clusters + 1]: cluster c's units are entries
+ *                   cluster_start[c] .. cluster_start[c + 1] - 1 of items
+ *   items         : out, int [5 * B*H*ceil(ceil(N/128)/2)]: per entry
+ *                   (bh, 2u, i0, n_it, rot), visiting Q tiles as in
+ *                   fattn_bwd_schedule_items
+ * Returns FATTN_ERR_INVALID_ARG for bad sizes, clusters < 1 or above the
+ * unit count, more than 2^24 units, or NULL outputs.
+ */
+int fattn_bwd_pair_schedule_items(int B, int H, int N, int causal, int clusters, long long l2_bytes,
+                                  int* cluster_start, int* items);
 
 /*
  * Synchronise `stream`, then report the first error since the last call:

@@ -10,7 +10,8 @@ import os
 import pytest
 
 from exact_attention_fattn_gb300 import _lib
-from exact_attention_fattn_gb300.attention import fattn_bwd_schedule, fattn_bwd_schedule_items
+from exact_attention_fattn_gb300.attention import (fattn_bwd_pair_schedule_items, fattn_bwd_schedule,
+                                                   fattn_bwd_schedule_items)
 
 L2 = 126 * 2**20  # an L2 of GB300's size (the head sections are sized from it)
 SMS = 152
@@ -213,3 +214,43 @@ def test_the_simulation_detects_a_cycle():
     # CTA 1, behind tile 1 on Q1, which needs tile 0 on Q1 -- last on CTA 0
     cyc = [[(0, 1, 0, 1, 0), (0, 0, 1, 1, 0)], [(0, 1, 1, 1, 0), (0, 0, 0, 1, 0)]]
     assert not ordered_reduction_finishes(cyc, 2, True)
+
+
+# ---------------------------------------------------------------------------
+# The CTA-pair backward: units of two K/V tiles dealt to clusters of two CTAs.
+
+PAIR_CASES = [
+    (2, 32, 4096, True),      # bench shape: paired units and a balancing tail
+    (1, 16, 16384, True),
+    (8, 16, 4096, False),     # head sections
+    (1, 3, 1920, True),       # 15 tiles: the last unit's second tile is past N
+    (1, 1, 128, False),       # one unit
+    (3, 5, 2000, True),
+    (4, 20, 512, True),
+]
+
+
+@pytest.mark.parametrize("B,H,N,causal", PAIR_CASES)
+def test_pair_schedule_every_unit_once(B, H, N, causal):
+    n_tiles = math.ceil(N / 128)
+    n_units = (n_tiles + 1) // 2
+    clusters = min(SMS // 2, B * H * n_units)
+    per = fattn_bwd_pair_schedule_items(B, H, N, causal, clusters, L2)
+    seen = {}
+    steps = []
+    for c, items in enumerate(per):
+        walked = 0
+        for bh, j, i0, n_it, rot in items:
+            assert j % 2 == 0 and 0 <= j < n_tiles
+            key = (bh, j // 2)
+            assert key not in seen, f"unit {key} scheduled twice"
+            seen[key] = c
+            assert n_it == (n_tiles - j if causal else n_tiles)
+            assert i0 == (j if causal else 0)
+            walked += n_it
+        steps.append(walked)
+    assert len(seen) == B * H * n_units
+    # the static deal leaves no cluster far behind the others
+    total = sum(steps)
+    if clusters > 1 and total >= 8 * clusters:
+        assert max(steps) <= 1.1 * total / clusters + n_tiles + 2
