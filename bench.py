@@ -294,6 +294,7 @@ def run_fattn(args, w):
     def finish():
         A.fattn_bwd_finish(ws, dq, scale=sc)
 
+    A.fattn_set_bwd_pair(args.bwd_pair)
     stages = [("fwd", fwd), ("bwd_prepare", prep), ("bwd_main", main), ("bwd_finish", finish)]
     for _ in range(args.warmup):
         for _, fn in stages:
@@ -465,6 +466,7 @@ def run_fattn(args, w):
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                    "causal": w.causal, "parallelism": f"replicas x{world}",
+                   "bwd_kernel": "cta_pair" if args.bwd_pair else "one_cta_per_tile",
                    "l2": "inputs larger than L2: q, k, v, o, dO take "
                          f"{5 * q.numel() * 2 / 2**20:.0f} MiB > 129 MB L2; no flush"},
         "frac_of_peak": value / world / peaks["bf16"],
@@ -659,6 +661,9 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the FP8 forward, deterministic backward and workload sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bwd-pair", action="store_true",
+                    help="time the CTA-pair backward kernel (fattn_set_bwd_pair) instead of the "
+                         "default one-CTA-per-tile kernel")
     ap.add_argument("--cpu-heads", type=int, default=32)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)      # at least three untimed warm-up steps
