@@ -19,14 +19,16 @@
 // CTAs in snake order, so that every CTA gets a similar total; the next item's
 // Q load and first S MMAs overlap the current item's last steps and
 // epilogue.
-//   warps 0-3  softmax for Q tile 0 (TMEM lanes 0..127, one row per thread)
-//   warps 4-7  softmax for Q tile 1
+//   warps 0-3  softmax of slot 0 (TMEM lanes 0..127, one row per thread)
+//   warps 4-7  softmax of slot 1
+// A slot is a Q buffer, its TMEM columns and barriers, and the warpgroup
+// that serves them; tile t of item m sits in slot slot_of(m, t).
 //   warp 8     TMEM allocation + MMA issue (converged warp, elected lane)
 //   warp 9     TMA producer (converged warp, elected lane)
 //   warps 10-11 idle
-// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d,256+2d);
-// P_t (bf16 pairs, 64 columns) aliases S_t at d = 128 and sits in
-// [384+64t, 448+64t) at d = 64.
+// TMEM (512 columns), by slot: S0 [0,128) S1 [128,256) O0 [256,256+d)
+// O1 [256+d,256+2d); P (bf16 pairs, 64 columns) aliases the slot's S at
+// d = 128 and sits in [384+64s, 448+64s) at d = 64.
 #include "fattn_internal.h"
 #include "fattn_ptx.cuh"
 
@@ -106,6 +108,22 @@ struct Item {
 template <bool CAUSAL>
 __device__ __forceinline__ int q_row0(const Item& w, int t) {
   return w.q0 + (CAUSAL ? 1 - t : t) * kBM;
+}
+
+template <int V>
+struct IntC {
+  static constexpr int value = V;
+};
+
+// Slot (TMEM columns, Q buffer, barriers, softmax warpgroup) of tile t in
+// item m.  With the causal mask the upper tile, which has one key tile more,
+// alternates between the two slots: the warpgroup whose lower tile finished
+// a key tile earlier takes the next item's upper tile while the other one
+// writes its epilogue (measured on GB300: 195.7-196.4 -> 193.4-193.7 us on
+// B = 2, H = 32, N = 4096; unmasked runs keep t = slot).
+template <bool CAUSAL>
+__device__ __forceinline__ int slot_of(int m, int t) {
+  return CAUSAL ? (t ^ (m & 1)) : t;
 }
 
 // The m-th work item of this CTA: items are numbered in sections of
@@ -204,14 +222,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 8) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     // ================================================================ softmax
-    const int t = warp >> 2;
+    const int sl = warp >> 2;             // this warpgroup's slot
     const int wq = warp & 3;
     const int r_tile = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_off + C::col_s(t);
-    const uint32_t tP = tmem + lane_off + C::col_p(t);
-    const uint32_t tO = tmem + lane_off + C::col_o(t);
-    dcheck(C::col_s(t) + kBN <= 512 && C::col_o(t) + HD <= 512 && C::col_p(t) + 64 <= 512 &&
+    const uint32_t tS = tmem + lane_off + C::col_s(sl);
+    const uint32_t tP = tmem + lane_off + C::col_p(sl);
+    const uint32_t tO = tmem + lane_off + C::col_o(sl);
+    dcheck(C::col_s(sl) + kBN <= 512 && C::col_o(sl) + HD <= 512 && C::col_p(sl) + 64 <= 512 &&
                ((tmem >> 16) & 0xFFFFu) == 0u,
            args.status, 301);
     float c = args.scale_log2;   // FP8: times the Q and K block scales, per tile pair
@@ -222,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     Item w;
     for (int m = 0; ok && get_item<CAUSAL>(m, N, BH, args.sec_heads, w); ++m) {
+      const int t = slot_of<CAUSAL>(m, sl);   // the item's tile in this slot (involution)
       const int nj = w.n[t];
       if (nj == 0) continue;
       const int qs = q_row0<CAUSAL>(w, t);
@@ -259,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           lrho = fmaxf(__log2f(rho), -100.f);
           inv_rho = ex2_approx(-lrho);
         }
-        ok = __all_sync(0xffffffffu, mbar_wait(b.s_full[t], s_count & 1, wc, kWaitSFull));
+        ok = __all_sync(0xffffffffu, mbar_wait(b.s_full[sl], s_count & 1, wc, kWaitSFull));
         if (!ok) break;
         ++s_count;
         tc_fence_after();
@@ -386,13 +405,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(b.p_full[t]);
+        mbar_arrive(b.p_full[sl]);
       }
       if (!ok) break;
       // ---- epilogue: O / l_bf -> bf16 to global, L = (m + log2 l) ln 2.  O_t
       // is read out of TMEM whole (each thread its own row) and handed back
       // to the MMA warp before the stores.
-      ok = __all_sync(0xffffffffu, mbar_wait(b.o_full[t], o_count & 1, wc, kWaitOFull));
+      ok = __all_sync(0xffffffffu, mbar_wait(b.o_full[sl], o_count & 1, wc, kWaitOFull));
       if (!ok) break;
       ++o_count;
       tc_fence_after();
@@ -413,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(b.o_empty[t]);
+      mbar_arrive(b.o_empty[sl]);
       // Stores of whole 128-byte lines.  Row-per-thread stores would put 32
       // lines into every warp store, 16 bytes each, and the L1 traffic they
       // cause slows the MMAs' shared-memory operand reads (measured on GB300:
@@ -512,20 +531,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       uint32_t kvb = 0;                      // ring index of this item's first K tile
-      uint32_t p_count[2] = {0u, 0u};        // P_t tiles consumed (phase of p_full)
-      uint32_t o_count[2] = {0u, 0u};        // items finished per tile (phase of o_empty)
-      Item w;
-      for (int m = 0; get_item<CAUSAL>(m, N, BH, args.sec_heads, w); ++m) {
+      // Per tile of the current item (kept in registers: the slots' counters
+      // trade places whenever the slot mapping does).
+      uint32_t p_count[2] = {0u, 0u};        // P tiles consumed in the tile's slot (p_full phase)
+      uint32_t o_count[2] = {0u, 0u};        // items finished in the tile's slot (o_empty phase)
+      Item w{};
+      // One item; F = the slot of the upper tile, a compile-time constant so
+      // that every TMEM column and shared-memory address below folds.
+      auto run_item = [&](auto f_c, int m) -> bool {
+        constexpr int F = decltype(f_c)::value;
         const int nt = w.nt;
-        if (!mbar_wait_warp(b.q_full, m & 1, wc, kWaitQFull)) goto mma_end;
-        if (!mbar_wait_warp(kv_full(kvb), kv_parity(kvb), wc, kWaitKvFull)) goto mma_end;
+        if (!mbar_wait_warp(b.q_full, m & 1, wc, kWaitQFull)) return false;
+        if (!mbar_wait_warp(kv_full(kvb), kv_parity(kvb), wc, kWaitKvFull)) return false;
         tc_fence_after();
-        // S_t(0) may overwrite S_t / P_t: the previous item's P V MMAs that
-        // read P_t were issued earlier, and MMAs complete in issue order.
+        // S(0) may overwrite the slot's S / P: the previous item's P V MMAs
+        // that read P there were issued earlier, and MMAs complete in issue
+        // order.
+#pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (w.n[t] > 0) {
-            issue_s(t, kvb);
-            mma_commit_w(b.s_full[t]);
+            issue_s(t ^ F, kvb);
+            mma_commit_w(b.s_full[t ^ F]);
           }
         }
         mma_commit_w(kv_empty(kvb));
@@ -533,33 +559,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < nt; ++j) {
           const uint32_t iv = kvb + 2 * j + 1;
           const uint32_t ikn = kvb + 2 * j + 2;
-          if (!mbar_wait_warp(kv_full(iv), kv_parity(iv), wc, kWaitKvFull)) goto mma_end;
+          if (!mbar_wait_warp(kv_full(iv), kv_parity(iv), wc, kWaitKvFull)) return false;
+#pragma unroll
           for (int t = 0; t < 2; ++t) {
+            const int sl = t ^ F;
             if (j < w.n[t]) {
               if (j == 0 && o_count[t] > 0 &&
-                  !mbar_wait_warp(b.o_empty[t], (o_count[t] - 1) & 1, wc, kWaitOFull))
-                goto mma_end;   // the previous item's O_t has been read out
-              if (!mbar_wait_warp(b.p_full[t], p_count[t] & 1, wc, kWaitPFull)) goto mma_end;
+                  !mbar_wait_warp(b.o_empty[sl], (o_count[t] - 1) & 1, wc, kWaitOFull))
+                return false;   // the slot's previous O has been read out
+              if (!mbar_wait_warp(b.p_full[sl], p_count[t] & 1, wc, kWaitPFull)) return false;
               ++p_count[t];
               tc_fence_after();
-              issue_pv(t, iv, j > 0 ? 1u : 0u);
-              if (j == w.n[t] - 1) mma_commit_w(b.o_full[t]);
+              issue_pv(sl, iv, j > 0 ? 1u : 0u);
+              if (j == w.n[t] - 1) mma_commit_w(b.o_full[sl]);
             }
             if (t == 0 && j + 1 < nt) {
-              if (!mbar_wait_warp(kv_full(ikn), kv_parity(ikn), wc, kWaitKvFull)) goto mma_end;
+              if (!mbar_wait_warp(kv_full(ikn), kv_parity(ikn), wc, kWaitKvFull)) return false;
               tc_fence_after();
             }
             if (j + 1 < w.n[t]) {
-              issue_s(t, ikn);
-              mma_commit_w(b.s_full[t]);
+              issue_s(sl, ikn);
+              mma_commit_w(b.s_full[sl]);
             }
           }
           mma_commit_w(kv_empty(iv));
           if (j + 1 < nt) mma_commit_w(kv_empty(ikn));
           if (j + 2 == nt) mma_commit_w(b.q_empty);   // the last S MMAs are issued
         }
+        return true;
+      };
+      for (int m = 0; get_item<CAUSAL>(m, N, BH, args.sec_heads, w); ++m) {
+        if (CAUSAL && m > 0) {
+          // The slot mapping flips every item; the counters follow the slots.
+          uint32_t x = p_count[0];
+          p_count[0] = p_count[1];
+          p_count[1] = x;
+          x = o_count[0];
+          o_count[0] = o_count[1];
+          o_count[1] = x;
+        }
+        const bool item_ok = (CAUSAL && (m & 1)) ? run_item(IntC<1>{}, m) : run_item(IntC<0>{}, m);
+        if (!item_ok) goto mma_end;
         for (int t = 0; t < 2; ++t) o_count[t] += w.n[t] > 0 ? 1u : 0u;
-        kvb += 2 * nt;
+        kvb += 2 * w.nt;
       }
     mma_end:
       // No MMA may still be running when TMEM is released.
@@ -583,8 +625,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
           if (w.n[t] == 0) continue;
           for (int cc = 0; cc < C::kChunks; ++cc)
-            tma_load_3d_w(sbase + C::kQOff + t * C::kTileBytes + cc * C::kChunkBytes, &tm_q,
-                          b.q_full, cc * C::kChunkElems, q_row0<CAUSAL>(w, t), w.bh);
+            tma_load_3d_w(sbase + C::kQOff + slot_of<CAUSAL>(m, t) * C::kTileBytes +
+                              cc * C::kChunkBytes,
+                          &tm_q, b.q_full, cc * C::kChunkElems, q_row0<CAUSAL>(w, t), w.bh);
         }
         items = m + 1;
         bool aborted = false;
