@@ -7,8 +7,9 @@
 //   P^T  = 2^(S^T*scale*log2e - L_i*log2e)    (one thread per kv row and query half; bf16 back to TMEM)
 //   dP^T = V_j dO_i^T                   (tcgen05)
 //   dS^T = P^T o (dP^T - D_i)           (bf16 to TMEM and, as dS, to shared memory)
-//   dV_j += P^T dO_i,  dK_j += dS^T Q_i (tcgen05, accumulators in TMEM)
+//   dV_j += P^T dO_i                    (tcgen05, accumulator in TMEM)
 //   dQ_i  = dS K_j                      (tcgen05) -> fp32 reduce-adds into dq_accum
+//   dK_j += dS^T Q_i                    (tcgen05, issued after dQ: see below)
 // At the end of an item dK_j * scale and dV_j are stored as bf16.  dQ = scale *
 // dq_accum is converted by a separate kernel.  The dQ and dK formulas follow
 // from S = scale Q K^T by the chain rule (the pages stop at dS).
@@ -38,13 +39,20 @@
 // every key row (P and dS are elementwise, so the halves never exchange
 // anything); 8 TMEM allocation + MMA issue; 9 TMA producer; 10 dQ reduce;
 // 11 idle; 12-15 dQ parking.
-// TMEM (512 columns): A [0,128) holds S^T, then P^T; B [128,256) holds dP^T,
-// then dS^T, then dQ ([128,128+d)).  Each warpgroup packs its 64 bf16 values
-// (32 columns) into the first half of the 64 fp32 columns it read itself
-// (query 0-63 -> [0,32), query 64-127 -> [64,96)), never into columns the
-// other warpgroup may still be reading.
-// dV at [256,256+d), dK at [256+d,256+2d).  With dQ in B, the next S^T can be
-// computed into A while the dQ rows are being read out.
+// TMEM (512 columns): A [0,128) holds S^T, then P^T and dS^T; B [128,256)
+// holds dP^T, then dQ ([128,128+d)).  Each warpgroup packs its 64 bf16
+// values of P^T (32 columns) into the first half of the 64 fp32 columns of
+// S^T it read itself (query 0-63 -> [0,32), query 64-127 -> [64,96)) and
+// its dS^T into the second half ([32,64), [96,128)), never into columns the
+// other warpgroup may still be reading.  dV at [256,256+d), dK at
+// [256+d,256+2d).
+// With dS^T out of B, dQ can be computed into B as soon as dS is complete,
+// before dK: the chain dS -> dQ -> dQ parked -> next dP^T -> next dS sets the
+// pace of a step (a clock64 trace: ~4600 cycles against 2560 of MMA), and dK
+// now runs while dQ is being parked (measured on GB300: whole backward 645-647
+// -> 622-626 us on B = 2, H = 32, N = 4096 causal, 2-3 % on the other
+// shapes).  With dQ in B, the next S^T can be computed into A while the dQ
+// rows are being read out.
 #include "fattn_internal.h"
 #include "fattn_ptx.cuh"
 #include "fattn_sched.h"
@@ -87,7 +95,7 @@ struct BwdCfg {
   static constexpr int kDsBytes = kTile * kTile * 2;
   static constexpr int kLdOff = kDsOff + kDsBytes;  // stage s: L2[128], D[128]
   static constexpr int kBarOff = kLdOff + 2 * 1024;
-  static constexpr int kNumBars = 22;
+  static constexpr int kNumBars = 23;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16;
   static constexpr uint32_t kColDK = kColDV + HD;
@@ -119,6 +127,8 @@ enum : int {
   kBarVEmpty = 19,   // the item's last MMA reading V_j has completed
   kBarDkvEmpty = 20, // dK_j / dV_j have been read out of TMEM
   kBarDqEmpty1 = 21, // dQ-parked of the steps that use stage 1
+  kBarDkDone = 22,   // the step's dK MMA (the last reader of Q_i) has completed
+                     // (phase = step parity)
 };
 
 // dQ-parked barrier of a step: one per Q/dO stage, so that each completes
@@ -192,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarDqEmpty), kParkThreads);
     mbar_init(bar(kBarDqEmpty1), kParkThreads);
     mbar_init(bar(kBarDkvFull), 1);
+    mbar_init(bar(kBarDkDone), 1);
     mbar_init(bar(kBarMmaDone), 1);
     misc[1] = 0u;
     fence_barrier_init();
@@ -311,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[e / 2] = pack_bf16x2(__uint_as_float(y[0]), __uint_as_float(y[1]));
             pk[e / 2 + 1] = pack_bf16x2(__uint_as_float(y[2]), __uint_as_float(y[3]));
           }
-          tmem_st16(tB + col0 + 16 * g, pk);
+          tmem_st16(tA + col0 + 32 + 16 * g, pk);
           // dS row r, query columns [col0 + 32g, +32) = four 16-byte chunks of
           // the MN-major (query-contiguous) operand: 64-column atoms, 128-byte
           // swizzle inside each.
@@ -454,9 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_tmem_a(tmem + kColDV, kColA, sDo(s), acc);           // dV += P^T dO
           if (!mbar_wait_warp(bar(kBarDsFull), ph, wc, kWaitDsFull)) goto mma_end;
           tc_fence_after();
-          mma_tmem_a(tmem + C::kColDK, kColB, sQ(s), acc);         // dK += dS^T Q
-          // dQ = dS K into B (dS^T there has just been consumed by the dK MMA,
-          // issued before): A = dS (q contiguous, MN-major), B = K (HD contiguous).
+          // dQ = dS K into B first (the compute warps have read dP^T out of
+          // it), so that its parking overlaps the dK product: A = dS (q
+          // contiguous, MN-major), B = K (HD contiguous).
           {
             const uint64_t dds = sdesc_sw128(sDs, 16384, 1024);
             const uint64_t dk = sdesc_sw128(sK, C::kChunkBytes, 1024);
@@ -467,6 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           mma_commit_w(bar(kBarDqFull));
+          mma_tmem_a(tmem + C::kColDK, kColA + 32, sQ(s), acc);    // dK += dS^T Q
+          mma_commit_w(bar(kBarDkDone));
           if (it + 1 < n_it) {
             if (!qfull(step + 1)) goto mma_end;
             tc_fence_after();
@@ -649,9 +662,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kParkRegs));
     // ================================================================ dQ parking
     // For each step: dQ_i rows (TMEM lane = query row), all d columns -> the
-    // Q/dO stage of the step (free now: every MMA that read it has
-    // completed), as 32 x 32 fp32 boxes with the 128-byte swizzle.  Query
-    // rows 0-63 land in the stage's Q half, 64-127 in its dO half.
+    // Q/dO stage of the step, as 32 x 32 fp32 boxes with the 128-byte
+    // swizzle.  Query rows 64-127 land in the stage's dO half (its readers,
+    // dP^T and dV, completed before dQ), rows 0-63 in its Q half once the
+    // step's dK MMA, issued after dQ, has completed too.
     const int wq = warp & 3;
     const uint32_t tB = tmem + (static_cast<uint32_t>(wq * 32) << 16) + kColB;
     bool ok = true;
@@ -660,6 +674,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int m = 0; ok && get_bwd_item<CAUSAL>(m, n_tiles, args, w); ++m) {
       for (int it = 0; it < w.n_it; ++it, ++step) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDqFull), step & 1, wc, kWaitDqFull));
+        // Query rows 0-63 go to the stage's Q half, which the step's dK MMA
+        // (issued after dQ) may still be reading.
+        if (ok && wq < 2)
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarDkDone), step & 1, wc, kWaitDqFull));
         if (!ok) break;
         tc_fence_after();
         const uint32_t stage = sbase + C::kStageOff + (step & 1) * C::kStageBytes;
