@@ -9,6 +9,9 @@ is compared with it:
   H = 32): forward and backward, all 64 heads, every element;
 * the non-causal d = 128 sweep (B = 8, H = 16, values 0.5 N(0,1)) at
   N = 512, 1024 and 2048: forward, all 128 heads, every element;
+* the non-causal d = 64 workload (B = 4, H = 16, N = 1024) and the
+  non-causal N = 4096, d = 128 shape of the benchmark's sweep (B = 2,
+  H = 32): forward and backward, every head, every element;
 * the FP8 forward on the causal outlier workload: every element, against the
   exact attention of its dequantized inputs;
 * the long-context causal workload (B = 1, H = 16, N = 16384): O, L and dQ on
@@ -69,6 +72,35 @@ def test_causal_outliers_every_element():
     big_q = np.abs(to_np(inp["q"])).max(axis=-1) > 20.0
     check_o(o[big_q], ref[0][big_q], "O x20 rows", abs_weighted=a[big_q])
     check_l(lse[big_q], ref[1][big_q], "L x20 rows")
+
+
+def _every_element_fwd_bwd(w, tag):
+    inp = W.make_inputs(w)
+    got = _gpu_fwd_bwd(inp, w.causal, w.scale)
+    torch.cuda.synchronize()
+    ref = [np.empty_like(g) for g in got] + [np.empty_like(got[0])]
+    jobs = [OP.head_slice(inp, hf, w.H, ("q", "k", "v", "do")) + (w.causal, w.scale)
+            for hf in range(w.B * w.H)]
+    with OP.pool() as p:
+        for hf, res in enumerate(p.imap(OP.head_forward_backward, jobs)):
+            b, h = divmod(hf, w.H)
+            for dst, r in zip(ref, res):
+                dst[b, h] = r
+    o, lse, dq, dk, dv = got
+    check_o(o, ref[0], f"O {tag}", abs_weighted=ref[5])
+    check_l(lse, ref[1], f"L {tag}")
+    check_grad(dq, ref[2], f"dQ {tag}")
+    check_grad(dk, ref[3], f"dK {tag}")
+    check_grad(dv, ref[4], f"dV {tag}")
+
+
+def test_d64_workload_every_element():
+    _every_element_fwd_bwd(W.MEDIUM_D64, "d=64")
+
+
+def test_noncausal_n4096_every_element():
+    w = W.Workload("b2h32_n4096_d128", 2, 32, 4096, 128, False, seed=1005)
+    _every_element_fwd_bwd(w, "non-causal N=4096")
 
 
 @pytest.mark.parametrize("n", W.SWEEP_NS)
