@@ -16,6 +16,12 @@ below ``entry_outlier_frac`` are replaced by that normal times
 block scales handle worst).  Finally every tensor is rounded to bf16
 (round-to-nearest-even, torch ``.to``).
 
+``make_inputs_device`` draws the same recipe (without outlier rows) with a
+generator on the GPU, for shapes too large to draw on the host: Q, K, V
+(and dO) in that order, each a standard normal tensor in fp32 times
+``value_scale``, rounded to bf16.  Its bytes differ from ``make_inputs``'s
+(another generator); the oracle is given slices of the same tensors.
+
 ``random_signs`` draws the +-1 diagonal of the random orthogonal matrix used
 for incoherent processing before FP8 quantization.
 """
@@ -92,6 +98,26 @@ def make_inputs(w: Workload, seed: int | None = None, with_grad: bool | None = N
             z = torch.randn(shape, generator=g, dtype=torch.float32) * w.entry_outlier_std
             t[name] = torch.where(u < w.entry_outlier_frac, z, t[name])
     return {n: x.to(torch.bfloat16).contiguous() for n, x in t.items()}
+
+
+def make_inputs_device(w: Workload, device, seed: int | None = None,
+                       with_grad: bool | None = None):
+    """Return dict(q, k, v[, do]) of contiguous bf16 tensors [B,H,N,d] on ``device``."""
+    if w.outlier_frac > 0 or w.entry_outlier_frac > 0:
+        raise ValueError("make_inputs_device draws no outliers")
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed if seed is None else seed)
+    shape = (w.B, w.H, w.N, w.d)
+    names = ["q", "k", "v"]
+    if w.backward if with_grad is None else with_grad:
+        names.append("do")
+    out = {}
+    for n in names:
+        x = torch.randn(shape, generator=g, dtype=torch.float32, device=device)
+        x.mul_(w.value_scale)
+        out[n] = x.to(torch.bfloat16).contiguous()
+        del x
+    return out
 
 
 def random_signs(d: int, seed: int) -> torch.Tensor:

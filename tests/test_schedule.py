@@ -47,6 +47,10 @@ CASES = [
     (3, 5, 2000, 64, True, False),      # ragged N, small grid
     (4, 8, 1024, 128, False, True),
     (16, 16, 1024, 128, True, False),
+    # the size-limit shapes of the GPU parity tests (just under 2^31 elements)
+    (128, 128, 1023, 128, False, False),
+    (128, 128, 1023, 128, True, False),
+    (256, 128, 1023, 64, False, False),
 ]
 
 
