@@ -534,8 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (grow0 + j < N &&
               dcheck(o_idx + 8 <= static_cast<size_t>(BH) * N * HD, args.status, 302)) {
             uint4* dst = reinterpret_cast<uint4*>(args.o + o_idx);
-            *dst = make_uint4(pw[4 * (8 * h + j)], pw[4 * (8 * h + j) + 1],
-                              pw[4 * (8 * h + j) + 2], pw[4 * (8 * h + j) + 3]);
+            __stcs(dst, make_uint4(pw[4 * (8 * h + j)], pw[4 * (8 * h + j) + 1],
+                                   pw[4 * (8 * h + j) + 2], pw[4 * (8 * h + j) + 3]));
           }
         }
       }
@@ -698,6 +698,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       uint32_t kvb = 0;      // ring index of the next K/V load
       int items = 0;
+      // Q is read once; K and V are read again by the other Q-tile pairs of
+      // the head: keep them in L2 ahead of Q and O (O is stored with the
+      // streaming hint).  Measured on GB300, B = 2, H = 32, N = 4096 causal:
+      // DRAM 594 -> 571 MB per launch, time unchanged.
+      const uint64_t pol_q = l2_evict_first_policy();
+      const uint64_t pol_kv = l2_evict_last_policy();
       Item w;
       for (int m = 0; get_item<CAUSAL>(m, N, BH, args.sec_heads, w); ++m) {
         if (m > 0 && !mbar_wait_warp(b.q_empty, (m - 1) & 1, wc, kWaitKvEmpty)) break;
@@ -707,9 +713,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
           if (w.n[t] == 0) continue;
           for (int cc = 0; cc < C::kChunks; ++cc)
-            tma_load_3d_w(sbase + C::kQOff + slot_of<CAUSAL>(m, t) * C::kTileBytes +
-                              cc * C::kChunkBytes,
-                          &tm_q, b.q_full, cc * C::kChunkElems, q_row0<CAUSAL>(w, t), w.bh);
+            tma_load_3d_hint_w(sbase + C::kQOff + slot_of<CAUSAL>(m, t) * C::kTileBytes +
+                                   cc * C::kChunkBytes,
+                               &tm_q, b.q_full, cc * C::kChunkElems, q_row0<CAUSAL>(w, t), w.bh,
+                               pol_q);
         }
         items = m + 1;
         bool aborted = false;
@@ -731,11 +738,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                  304);
           if (FP8 && (i & 1)) {
             // transposed V: d rows x 128 key bytes starting at key (i/2)*128
-            tma_load_3d_w(dst, tm, full, (i >> 1) * kBN, 0, w.bh);
+            tma_load_3d_hint_w(dst, tm, full, (i >> 1) * kBN, 0, w.bh, pol_kv);
           } else {
             for (int cc = 0; cc < C::kChunks; ++cc)
-              tma_load_3d_w(dst + cc * C::kChunkBytes, tm, full, cc * C::kChunkElems,
-                            (i >> 1) * kBN, w.bh);
+              tma_load_3d_hint_w(dst + cc * C::kChunkBytes, tm, full, cc * C::kChunkElems,
+                                 (i >> 1) * kBN, w.bh, pol_kv);
           }
         }
         if (aborted) break;

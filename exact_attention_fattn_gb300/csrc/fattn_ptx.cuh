@@ -367,6 +367,30 @@ __device__ __forceinline__ void tma_load_3d_w(uint32_t dst, const void* tmap, ui
       : "memory");
 }
 
+// L2 eviction policies for the cache-hint forms of the TMA copies.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_load_3d_w with an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d_hint_w(uint32_t dst, const void* tmap, uint32_t bar,
+                                                   int c0, int c1, int c2, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_load_1d_w(uint32_t dst, const void* src, uint32_t bytes,
                                                uint32_t bar) {
   asm volatile(
