@@ -367,6 +367,16 @@ __device__ __forceinline__ void tma_load_3d_w(uint32_t dst, const void* tmap, ui
       : "memory");
 }
 
+// tma_reduce_add_3d with an L2 cache policy.
+__device__ __forceinline__ void tma_reduce_add_3d_hint(const void* tmap, uint32_t src, int c0,
+                                                       int c1, int c2, uint64_t policy) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3, %4}], [%1], %5;" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+
 // L2 eviction policies for the cache-hint forms of the TMA copies.
 __device__ __forceinline__ uint64_t l2_evict_last_policy() {
   uint64_t p;
