@@ -23,7 +23,12 @@
 // heaviest first (causal: the pairs with the most key tiles) and dealt to the
 // CTAs in snake order, so that every CTA gets a similar total; the next item's
 // Q load and first S MMAs overlap the current item's last steps and
-// epilogue.
+// epilogue.  Without the mask each slot's Q buffer has its own full / empty
+// barrier pair and is refilled as soon as its tile has had its last S, in
+// the order Q(tile 0), K_0, Q(tile 1), V_0, ... (measured on GB300 against
+// one pair for both buffers, outputs bit-identical: B = 8, H = 16, N = 4096
+// 701-708 -> 676-683 us, d = 64 N = 4096 297 -> 293 us); the causal items
+// keep one pair for both (see the loader).
 //   warps 0-3  softmax of slot 0 (TMEM lanes 0..127, one row per thread)
 //   warps 4-7  softmax of slot 1
 // A slot is a Q buffer, its TMEM columns and barriers, and the warpgroup
@@ -87,8 +92,8 @@ struct FwdCfg {
   static constexpr int kKvOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKvOff + kStages * kTileBytes;
   // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2],
-  // o_empty[2], mma_done, s_read[2], pv_done[2]
-  static constexpr int kNumBars = 2 + 2 * kStages + 8 + 1 + 4;
+  // o_empty[2], mma_done, s_read[2], pv_done[2], q_full[1], q_empty[1]
+  static constexpr int kNumBars = 2 + 2 * kStages + 8 + 1 + 4 + 2;
   // P has columns of its own (d = 64): the next S can be computed while the
   // softmax still works on the current one.
   static constexpr bool kEarlyS = !FP8 && HD == 64;
@@ -196,6 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // kEarlyS only: S read into registers / P V complete, per slot.
   auto s_read_bar = [&](int t) { return rest + 72u + 8u * t; };
   auto pv_done_bar = [&](int t) { return rest + 88u + 8u * t; };
+  // Q tile of slot s landed / free again (one pair per slot).
+  auto q_full_bar = [&](int sl) { return sl ? rest + 104u : b.q_full; };
+  auto q_empty_bar = [&](int sl) { return sl ? rest + 112u : b.q_empty; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
 
   const int warp = threadIdx.x >> 5;
@@ -206,6 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(b.q_full, 1);
     mbar_init(b.q_empty, 1);
+    mbar_init(rest + 104u, 1);
+    mbar_init(rest + 112u, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(b.kv_full0 + 8 * s, 1);
       mbar_init(b.kv_empty0 + 8 * s, 1);
@@ -599,27 +609,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       // trade places whenever the slot mapping does).
       uint32_t p_count[2] = {0u, 0u};        // P tiles consumed in the tile's slot (p_full phase)
       uint32_t o_count[2] = {0u, 0u};        // items finished in the tile's slot (o_empty phase)
+      uint32_t qm[2] = {0u, 0u};             // Q tiles consumed per slot (q_full phase)
       Item w{};
       // One item; F = the slot of the upper tile, a compile-time constant so
       // that every TMEM column and shared-memory address below folds.
       auto run_item = [&](auto f_c, int m) -> bool {
         constexpr int F = decltype(f_c)::value;
         const int nt = w.nt;
-        if (!mbar_wait_warp(b.q_full, m & 1, wc, kWaitQFull)) return false;
-        if (!mbar_wait_warp(kv_full(kvb), kv_parity(kvb), wc, kWaitKvFull)) return false;
-        tc_fence_after();
         // S(0) may overwrite the slot's S / P: the previous item's P V MMAs
         // that read P there were issued earlier, and MMAs complete in issue
         // order.
+        bool k0_ready = false;
+        if constexpr (CAUSAL) {   // one Q barrier pair for both buffers (see the loader)
+          if (!mbar_wait_warp(b.q_full, m & 1, wc, kWaitQFull)) return false;
+        }
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (w.n[t] > 0) {
-            issue_s(t ^ F, kvb);
-            mma_commit_w(b.s_full[t ^ F]);
+            const int sl = t ^ F;
+            if constexpr (!CAUSAL) {
+              if (!mbar_wait_warp(q_full_bar(sl), qm[sl] & 1, wc, kWaitQFull)) return false;
+              ++qm[sl];
+            }
+            if (!k0_ready) {
+              if (!mbar_wait_warp(kv_full(kvb), kv_parity(kvb), wc, kWaitKvFull)) return false;
+              k0_ready = true;
+            }
+            tc_fence_after();
+            issue_s(sl, kvb);
+            mma_commit_w(b.s_full[sl]);
+            if (!CAUSAL && w.n[t] == 1) mma_commit_w(q_empty_bar(sl));   // the tile's only S
           }
         }
         mma_commit_w(kv_empty(kvb));
-        if (nt == 1) mma_commit_w(b.q_empty);   // every S MMA of the item is issued
+        if (CAUSAL && nt == 1) mma_commit_w(b.q_empty);   // every S MMA of the item is issued
         for (int j = 0; j < nt; ++j) {
           const uint32_t iv = kvb + 2 * j + 1;
           const uint32_t ikn = kvb + 2 * j + 2;
@@ -639,6 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j + 1 < w.n[t]) {
                   issue_s(sl, ikn);
                   mma_commit_w(b.s_full[sl]);
+                  if (!CAUSAL && j + 2 == w.n[t]) mma_commit_w(q_empty_bar(sl));   // the tile's last S
                 }
               }
             }
@@ -661,12 +685,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (j + 1 < w.n[t]) {
                 issue_s(sl, ikn);
                 mma_commit_w(b.s_full[sl]);
+                if (!CAUSAL && j + 2 == w.n[t]) mma_commit_w(q_empty_bar(sl));   // the tile's last S
               }
             }
           }
           mma_commit_w(kv_empty(iv));
           if (j + 1 < nt) mma_commit_w(kv_empty(ikn));
-          if (j + 2 == nt) mma_commit_w(b.q_empty);   // the last S MMAs are issued
+          if (CAUSAL && j + 2 == nt) mma_commit_w(b.q_empty);   // the last S MMAs are issued
         }
         return true;
       };
@@ -697,7 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Converged warp; one elected lane issues each copy.
     {
       uint32_t kvb = 0;      // ring index of the next K/V load
-      int items = 0;
+      uint32_t ql[2] = {0u, 0u};   // unmasked: Q tiles loaded per slot
+      int items = 0;               // causal: items whose Q pair was loaded
       // Q is read once; K and V are read again by the other Q-tile pairs of
       // the head: keep them in L2 ahead of Q and O (O is stored with the
       // streaming hint).  Measured on GB300, B = 2, H = 32, N = 4096 causal:
@@ -705,21 +731,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_q = l2_evict_first_policy();
       const uint64_t pol_kv = l2_evict_last_policy();
       Item w;
-      for (int m = 0; get_item<CAUSAL>(m, N, BH, args.sec_heads, w); ++m) {
-        if (m > 0 && !mbar_wait_warp(b.q_empty, (m - 1) & 1, wc, kWaitKvEmpty)) break;
-        uint32_t qbytes = 0;
-        for (int t = 0; t < 2; ++t) qbytes += w.n[t] > 0 ? C::kTileBytes : 0;
-        mbar_arrive_expect_tx_w(b.q_full, qbytes);
-        for (int t = 0; t < 2; ++t) {
-          if (w.n[t] == 0) continue;
+      bool aborted = false;
+      for (int m = 0; !aborted && get_item<CAUSAL>(m, N, BH, args.sec_heads, w); ++m) {
+        // Unmasked: Q of tile t into its slot once that slot's previous Q
+        // tile has had its last S, in the order Q(tile 0), K_0, Q(tile 1),
+        // V_0, ...  Causal: both Q tiles of the item once the previous item's
+        // last S MMAs are issued, then K_0 -- inside a forward + backward
+        // step the per-slot refill measured ~1 % slower for the causal mask
+        // (while faster for forward calls on their own).
+        auto load_q = [&](int t) -> bool {
+          if (w.n[t] == 0) return true;
+          const int sl = slot_of<CAUSAL>(m, t);
+          if (ql[sl] > 0 &&
+              !mbar_wait_warp(q_empty_bar(sl), (ql[sl] - 1) & 1, wc, kWaitKvEmpty))
+            return false;
+          mbar_arrive_expect_tx_w(q_full_bar(sl), C::kTileBytes);
           for (int cc = 0; cc < C::kChunks; ++cc)
-            tma_load_3d_hint_w(sbase + C::kQOff + slot_of<CAUSAL>(m, t) * C::kTileBytes +
-                                   cc * C::kChunkBytes,
-                               &tm_q, b.q_full, cc * C::kChunkElems, q_row0<CAUSAL>(w, t), w.bh,
+            tma_load_3d_hint_w(sbase + C::kQOff + sl * C::kTileBytes + cc * C::kChunkBytes, &tm_q,
+                               q_full_bar(sl), cc * C::kChunkElems, q_row0<CAUSAL>(w, t), w.bh,
                                pol_q);
+          ++ql[sl];
+          return true;
+        };
+        if constexpr (CAUSAL) {
+          if (m > 0 && !mbar_wait_warp(b.q_empty, (m - 1) & 1, wc, kWaitKvEmpty)) break;
+          uint32_t qbytes = 0;
+          for (int t = 0; t < 2; ++t) qbytes += w.n[t] > 0 ? C::kTileBytes : 0;
+          mbar_arrive_expect_tx_w(b.q_full, qbytes);
+          for (int t = 0; t < 2; ++t) {
+            if (w.n[t] == 0) continue;
+            for (int cc = 0; cc < C::kChunks; ++cc)
+              tma_load_3d_hint_w(sbase + C::kQOff + slot_of<CAUSAL>(m, t) * C::kTileBytes +
+                                     cc * C::kChunkBytes,
+                                 &tm_q, b.q_full, cc * C::kChunkElems, q_row0<CAUSAL>(w, t),
+                                 w.bh, pol_q);
+          }
+          items = m + 1;
+        } else {
+          if (!load_q(0)) break;
         }
-        items = m + 1;
-        bool aborted = false;
         for (int i = 0; i < 2 * w.nt; ++i) {
           const uint32_t r = kvb + i;
           const uint32_t s = r % C::kStages;
@@ -744,6 +794,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_3d_hint_w(dst + cc * C::kChunkBytes, tm, full, cc * C::kChunkElems,
                                  (i >> 1) * kBN, w.bh, pol_kv);
           }
+          if (!CAUSAL && i == 0 && !load_q(1)) {
+            aborted = true;
+            kvb = r + 1;
+            break;
+          }
         }
         if (aborted) break;
         kvb += 2 * w.nt;
@@ -752,6 +807,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t r = kvb > C::kStages ? kvb - C::kStages : 0; r < kvb; ++r)
         mbar_wait_drain(b.kv_full0 + 8u * (r % C::kStages), (r / C::kStages) & 1,
                         args.wait_budget);
+      for (int sl = 0; sl < 2; ++sl)
+        if (ql[sl] > 0) mbar_wait_drain(q_full_bar(sl), (ql[sl] - 1) & 1, args.wait_budget);
       if (items > 0) mbar_wait_drain(b.q_full, (items - 1) & 1, args.wait_budget);
     }
     __syncwarp();
