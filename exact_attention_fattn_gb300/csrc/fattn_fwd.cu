@@ -92,7 +92,8 @@ struct FwdCfg {
   static constexpr int kKvOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKvOff + kStages * kTileBytes;
   // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2],
-  // o_empty[2], mma_done, s_read[2], pv_done[2], q_full[1], q_empty[1]
+  // o_empty[2], mma_done, s_read[2], pv_done[2], and slot 1's own q_full /
+  // q_empty (unmasked items; causal items share the first pair)
   static constexpr int kNumBars = 2 + 2 * kStages + 8 + 1 + 4 + 2;
   // P has columns of its own (d = 64): the next S can be computed while the
   // softmax still works on the current one.
@@ -201,7 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // kEarlyS only: S read into registers / P V complete, per slot.
   auto s_read_bar = [&](int t) { return rest + 72u + 8u * t; };
   auto pv_done_bar = [&](int t) { return rest + 88u + 8u * t; };
-  // Q tile of slot s landed / free again (one pair per slot).
+  // Q tile of slot s landed / free again: one pair per slot for unmasked
+  // items; causal items use b.q_full / b.q_empty for both slots.
   auto q_full_bar = [&](int sl) { return sl ? rest + 104u : b.q_full; };
   auto q_empty_bar = [&](int sl) { return sl ? rest + 112u : b.q_empty; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
@@ -609,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // trade places whenever the slot mapping does).
       uint32_t p_count[2] = {0u, 0u};        // P tiles consumed in the tile's slot (p_full phase)
       uint32_t o_count[2] = {0u, 0u};        // items finished in the tile's slot (o_empty phase)
-      uint32_t qm[2] = {0u, 0u};             // Q tiles consumed per slot (q_full phase)
+      uint32_t qm[2] = {0u, 0u};             // unmasked: Q tiles consumed per slot (q_full phase)
       Item w{};
       // One item; F = the slot of the upper tile, a compile-time constant so
       // that every TMEM column and shared-memory address below folds.
