@@ -27,8 +27,9 @@
 // barrier pair and is refilled as soon as its tile has had its last S, in
 // the order Q(tile 0), K_0, Q(tile 1), V_0, ... (measured on GB300 against
 // one pair for both buffers, outputs bit-identical: B = 8, H = 16, N = 4096
-// 701-708 -> 676-683 us, d = 64 N = 4096 297 -> 293 us); the causal items
-// keep one pair for both (see the loader).
+// 701-708 -> 676-683 us, d = 64 N = 4096 297 -> 293 us; the FP8 forward
+// on B = 2, H = 32, N = 4096 causal 174.8-176.2 -> 172.6-172.8 us); the
+// causal bf16 items keep one pair for both (see the loader).
 //   warps 0-3  softmax of slot 0 (TMEM lanes 0..127, one row per thread)
 //   warps 4-7  softmax of slot 1
 // A slot is a Q buffer, its TMEM columns and barriers, and the warpgroup
@@ -181,6 +182,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
   using C = FwdCfg<HD, FP8>;
+  // Causal bf16 items share one Q barrier pair between the two buffers;
+  // unmasked and FP8 items refill each buffer as soon as its tile is done.
+  constexpr bool kSharedQ = CAUSAL && !FP8;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -622,14 +626,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // that read P there were issued earlier, and MMAs complete in issue
         // order.
         bool k0_ready = false;
-        if constexpr (CAUSAL) {   // one Q barrier pair for both buffers (see the loader)
+        if constexpr (kSharedQ) {   // one Q barrier pair for both buffers (see the loader)
           if (!mbar_wait_warp(b.q_full, m & 1, wc, kWaitQFull)) return false;
         }
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (w.n[t] > 0) {
             const int sl = t ^ F;
-            if constexpr (!CAUSAL) {
+            if constexpr (!kSharedQ) {
               if (!mbar_wait_warp(q_full_bar(sl), qm[sl] & 1, wc, kWaitQFull)) return false;
               ++qm[sl];
             }
@@ -640,11 +644,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             issue_s(sl, kvb);
             mma_commit_w(b.s_full[sl]);
-            if (!CAUSAL && w.n[t] == 1) mma_commit_w(q_empty_bar(sl));   // the tile's only S
+            if (!kSharedQ && w.n[t] == 1) mma_commit_w(q_empty_bar(sl));   // the tile's only S
           }
         }
         mma_commit_w(kv_empty(kvb));
-        if (CAUSAL && nt == 1) mma_commit_w(b.q_empty);   // every S MMA of the item is issued
+        if (kSharedQ && nt == 1) mma_commit_w(b.q_empty);   // every S MMA of the item is issued
         for (int j = 0; j < nt; ++j) {
           const uint32_t iv = kvb + 2 * j + 1;
           const uint32_t ikn = kvb + 2 * j + 2;
@@ -664,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j + 1 < w.n[t]) {
                   issue_s(sl, ikn);
                   mma_commit_w(b.s_full[sl]);
-                  if (!CAUSAL && j + 2 == w.n[t]) mma_commit_w(q_empty_bar(sl));   // the tile's last S
+                  if (!kSharedQ && j + 2 == w.n[t]) mma_commit_w(q_empty_bar(sl));   // the tile's last S
                 }
               }
             }
@@ -687,13 +691,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (j + 1 < w.n[t]) {
                 issue_s(sl, ikn);
                 mma_commit_w(b.s_full[sl]);
-                if (!CAUSAL && j + 2 == w.n[t]) mma_commit_w(q_empty_bar(sl));   // the tile's last S
+                if (!kSharedQ && j + 2 == w.n[t]) mma_commit_w(q_empty_bar(sl));   // the tile's last S
               }
             }
           }
           mma_commit_w(kv_empty(iv));
           if (j + 1 < nt) mma_commit_w(kv_empty(ikn));
-          if (CAUSAL && j + 2 == nt) mma_commit_w(b.q_empty);   // the last S MMAs are issued
+          if (kSharedQ && j + 2 == nt) mma_commit_w(b.q_empty);   // the last S MMAs are issued
         }
         return true;
       };
@@ -735,12 +739,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       Item w;
       bool aborted = false;
       for (int m = 0; !aborted && get_item<CAUSAL>(m, N, BH, args.sec_heads, w); ++m) {
-        // Unmasked: Q of tile t into its slot once that slot's previous Q
-        // tile has had its last S, in the order Q(tile 0), K_0, Q(tile 1),
-        // V_0, ...  Causal: both Q tiles of the item once the previous item's
-        // last S MMAs are issued, then K_0 -- inside a forward + backward
-        // step the per-slot refill measured ~1 % slower for the causal mask
-        // (while faster for forward calls on their own).
+        // Unmasked and FP8: Q of tile t into its slot once that slot's
+        // previous Q tile has had its last S, in the order Q(tile 0), K_0,
+        // Q(tile 1), V_0, ...  Causal bf16: both Q tiles of the item once the
+        // previous item's last S MMAs are issued, then K_0 -- inside a
+        // forward + backward step the per-slot refill measured ~1 % slower
+        // for the causal mask (while faster for forward calls on their own).
         auto load_q = [&](int t) -> bool {
           if (w.n[t] == 0) return true;
           const int sl = slot_of<CAUSAL>(m, t);
@@ -755,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++ql[sl];
           return true;
         };
-        if constexpr (CAUSAL) {
+        if constexpr (kSharedQ) {
           if (m > 0 && !mbar_wait_warp(b.q_empty, (m - 1) & 1, wc, kWaitKvEmpty)) break;
           uint32_t qbytes = 0;
           for (int t = 0; t < 2; ++t) qbytes += w.n[t] > 0 ? C::kTileBytes : 0;
@@ -796,7 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_3d_hint_w(dst + cc * C::kChunkBytes, tm, full, cc * C::kChunkElems,
                                  (i >> 1) * kBN, w.bh, pol_kv);
           }
-          if (!CAUSAL && i == 0 && !load_q(1)) {
+          if (!kSharedQ && i == 0 && !load_q(1)) {
             aborted = true;
             kvb = r + 1;
             break;
